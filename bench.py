@@ -1,0 +1,611 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized-gradient hot path on GB300.
+
+Default workload: one qgZ single-hop step (8 simulated ranks, gradients of
+one d=2048/ffn=5504 Llama-2 layer, block 256, LoCo error feedback s=1,
+beta=0.5): the error-feedback int4 quantization of every rank followed by
+the dequant-reduce of every destination shard.  Metric: gradient elements
+per second (R*N per step) through both kernels.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload qgz_single_hop|qgz_tiny|qgz_hierarchical|qwz|sr|all]
+
+One JSON line on rank 0 (per workload).  Under torchrun each rank runs an
+independent replica on its own GPU ("weak" scaling; the simulated ranks live
+in one GPU, there is no cross-GPU exchange); the time is the max over ranks.
+`--impl reference` times the CPU oracle (a plain single-threaded C
+statement of the same computation) on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from weight_communication_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "qgZ grad elements/s (EF-quant + dequant-reduce) and HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------------------
+# environment
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, use_cuda: bool):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("nccl" if use_cuda else "gloo")
+    return dist
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """Largest value across ranks (the job's time is the slowest rank's)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, dist, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return float(d["hbm_gbs"]), "measured"
+        except (ValueError, KeyError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cpu():
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return os.cpu_count() or 1, model
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (read-only)."""
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", str(period_ms)],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = Path(self.file.name).read_text().splitlines()
+        os.unlink(self.file.name)
+        sm, smax, reasons, n_all = [], [], set(), 0
+        for row in rows:
+            f = [x.strip() for x in row.split(",")]
+            if len(f) < 9:
+                continue
+            n_all += 1
+            try:
+                ts = _dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(self.REASONS, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# traffic figures from the committed ncu summaries
+# ---------------------------------------------------------------------------
+
+KERNEL_SOURCES = {
+    "ef_quant_int4": ["weight_communication_gb300/csrc/qgz_quant.cu",
+                      "weight_communication_gb300/csrc/wc_device.cuh"],
+    "dequant_reduce": ["weight_communication_gb300/csrc/qgz_reduce.cu",
+                       "weight_communication_gb300/csrc/wc_device.cuh"],
+    "dequant_reduce_requant": ["weight_communication_gb300/csrc/qgz_quant.cu",
+                               "weight_communication_gb300/csrc/wc_device.cuh"],
+    "qwz_quant_int8": ["weight_communication_gb300/csrc/qwz.cu",
+                       "weight_communication_gb300/csrc/wc_device.cuh"],
+    "qwz_dequant_int8": ["weight_communication_gb300/csrc/qwz.cu",
+                         "weight_communication_gb300/csrc/wc_device.cuh"],
+    "sr_accumulate": ["weight_communication_gb300/csrc/sr_accumulate.cu",
+                      "weight_communication_gb300/csrc/wc_device.cuh"],
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str, units: float):
+    """DRAM bytes per launch from profiles/traffic.txt, scaled to `units`
+    elements, or None when absent or taken on a different kernel source."""
+    p = ROOT / "profiles" / "traffic.txt"
+    if not p.exists():
+        return None
+    for line in p.read_text().splitlines():
+        f = line.split()
+        if len(f) < 5 or line.startswith("#"):
+            continue
+        k, wname, bytes_, units_measured, src = f[:5]
+        if k == kernel and wname == workload and src == kernel_source_hash(kernel):
+            return float(bytes_) * units / float(units_measured)
+    return None
+
+
+# ---------------------------------------------------------------------------
+# timed loops
+# ---------------------------------------------------------------------------
+
+def flush_l2(buf: torch.Tensor):
+    buf.add_(1)
+
+
+class Timer:
+    """CUDA events on the launching stream around every kernel of a step."""
+
+    def __init__(self, names, steps):
+        self.names = names
+        self.ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+                   for _ in range(steps)]
+
+    def mark(self, step, i):
+        self.ev[step][i].record()
+
+    def per_kernel_ms(self):
+        out = {}
+        for j, n in enumerate(self.names):
+            out[n] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in self.ev)
+        return out
+
+    def step_sum_ms(self):
+        return statistics.mean(e[0].elapsed_time(e[-1]) for e in self.ev)
+
+
+def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws):
+    from weight_communication_gb300.qgz import QgzReducer
+    out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+    red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev)
+    g_bytes = w.R * w.N * 2
+    nbatch = max(1, min(args.batches, (8 << 30) // g_bytes))
+    batches = [wl.qgz_gradients(w, t, device=dev) for t in range(nbatch)]
+    stream = torch.cuda.Stream(dev)
+    l2_resident = (w.R * w.N * (2 + 4 + 4) + w.N * 4) < 2 * L2_BYTES
+    flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev) if l2_resident else None
+    names = ["ef_quant_int4"] + (["dequant_reduce_requant"] if w.G > 1 else []) + ["dequant_reduce"]
+
+    def step(i, timer=None, ti=None):
+        g = batches[i % nbatch]
+        if timer is not None:
+            timer.mark(ti, 0)
+        red.quantize(g, stream)
+        if timer is not None:
+            timer.mark(ti, 1)
+        if w.G > 1:
+            from weight_communication_gb300 import binding
+            binding.dequant_reduce_requant(red.codes, red.scales, red.codes1, red.scales1,
+                                           w.N, w.R, w.G, w.B, stream)
+            if timer is not None:
+                timer.mark(ti, 2)
+            binding.dequant_reduce(red.codes1, red.scales1, red.out, w.N, w.R, w.G, w.B, 1.0, stream)
+        else:
+            from weight_communication_gb300 import binding
+            binding.dequant_reduce(red.codes, red.scales, red.out, w.N, w.R, 1, w.B, 1.0, stream)
+        if timer is not None:
+            timer.mark(ti, len(names))
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+            if flush is not None:
+                flush_l2(flush)
+        torch.cuda.synchronize(dev)
+        timer = Timer(names, args.steps)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sampler = ClockSampler(dev.index or 0) if args.clocks else None
+        time.sleep(0.2 if sampler else 0)
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        t0 = time.time()
+        start.record()
+        for i in range(args.steps):
+            step(args.warmup + i, timer, i)
+            if flush is not None:
+                flush_l2(flush)
+        end.record()
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        barrier(dist)
+        clocks = sampler.stop(t0, t1) if sampler else None
+    per_kernel = timer.per_kernel_ms()
+    # With an L2 flush between steps the flush is not part of the step: the
+    # step time is the kernels' event span; otherwise it is the whole region.
+    ms_local = timer.step_sum_ms() if flush is not None else start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local, dist, dev)
+    units = w.R * w.N
+    value = units * ws / (ms / 1e3)
+
+    # roofline of the dominant kernel (the error-feedback quantization)
+    peak, peak_kind = measured_peaks()
+    efq_bytes = w.R * w.N * (2 + 4 + 4 + 0.5) + w.R * w.N // w.B * 4
+    efq_ms = per_kernel["ef_quant_int4"]
+    achieved = efq_bytes / (efq_ms / 1e3) / 1e9
+    traffic = ncu_traffic("ef_quant_int4", w.name.split()[0], units)
+    kernels = {}
+    S = w.S
+    for n in names:
+        if n == "ef_quant_int4":
+            b = efq_bytes
+        elif n == "dequant_reduce_requant":
+            b = w.G * w.N * (w.L + 1) * (0.5 + 4 / w.B)
+        else:
+            nsrc = w.G if w.G > 1 else w.R
+            b = w.N * (nsrc * (0.5 + 4 / w.B) + (2 if w.out_bf16 else 4))
+        t = per_kernel[n]
+        kernels[n] = {"ms": round(t, 5), "algorithmic_bytes": int(b),
+                      "GB/s": round(b / (t / 1e3) / 1e9, 1),
+                      "frac": round(b / (t / 1e3) / 1e9 / peak, 4)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded normal gradients with sparse outliers)",
+        "config": {"workload": w.name, "R": w.R, "N": w.N, "G": w.G, "B": w.B,
+                   "err_scale": w.err_scale, "err_beta": w.err_beta,
+                   "out": "bf16" if w.out_bf16 else "fp32",
+                   "l2": ("flushed between steps (untimed 516 MB write)" if flush is not None
+                          else f"inputs exceed L2 ({units * 10 / 1e9:.1f} GB per step)"),
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": "ef_quant_int4", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": int(efq_bytes)},
+        "kernels": kernels,
+        "gpu_launches": args.steps * len(names),
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_qgz_e2e(w, red, batches[0], args, dev, dist, ws, stream)
+    return line, batches[0]
+
+
+def run_qgz_e2e(w, red, g_example, args, dev, dist, ws, stream):
+    """Same metric through the public API with host buffers: per step the
+    gradients go host -> device (pinned), both kernels run, and the reduced
+    shards come back device -> host, all inside the timed region."""
+    g_host = g_example.cpu().pin_memory()
+    out_host = torch.empty(red.out.shape, dtype=red.out.dtype).pin_memory()
+    g_dev = torch.empty_like(g_example)
+    steps = max(1, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            red.step_host(g_host, g_dev, out_host, stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(steps):
+            red.step_host(g_host, g_dev, out_host, stream)
+        end.record()
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+    ms = max_over_ranks(start.elapsed_time(end) / steps, dist, dev)
+    return {"value": w.R * w.N * ws / (ms / 1e3), "unit": "elements/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": g_host.numel() * g_host.element_size(),
+            "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+
+def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
+    from weight_communication_gb300 import binding
+    wd = wl.qwz_weights(w, device=dev)
+    codes = torch.empty(w.n, dtype=torch.int8, device=dev)
+    scales = torch.empty(w.n // w.B, dtype=torch.float32, device=dev)
+    back = torch.empty(w.n, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(dev)
+    names = ["qwz_quant_int8", "qwz_dequant_int8"]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            binding.qwz_quant_int8(wd, codes, scales, w.B, stream)
+            binding.qwz_dequant_int8(codes, scales, back, w.B, stream)
+        torch.cuda.synchronize(dev)
+        timer = Timer(names, args.steps)
+        barrier(dist)
+        for i in range(args.steps):
+            timer.mark(i, 0)
+            binding.qwz_quant_int8(wd, codes, scales, w.B, stream)
+            timer.mark(i, 1)
+            binding.qwz_dequant_int8(codes, scales, back, w.B, stream)
+            timer.mark(i, 2)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+    per = timer.per_kernel_ms()
+    ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
+    peak, kind = measured_peaks()
+    qb = w.n * (2 + 1) + w.n // w.B * 4
+    kernels = {n: {"ms": round(per[n], 5), "algorithmic_bytes": qb,
+                   "GB/s": round(qb / (per[n] / 1e3) / 1e9, 1),
+                   "frac": round(qb / (per[n] / 1e3) / 1e9 / peak, 4)} for n in names}
+    return {"metric": "qwZ weights/s (int8 quantize + dequantize round trip)",
+            "value": w.n * ws / (ms / 1e3), "unit": "weights/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0, 0.02) weights)",
+            "config": {"workload": w.name, "n": w.n, "B": w.B,
+                       "l2": f"inputs exceed L2 ({w.n * 6 / 1e9:.1f} GB per step)"},
+            "roofline": {"bound": "hbm", "kernel": "qwz_quant_int8",
+                         "achieved": kernels["qwz_quant_int8"]["GB/s"], "peak": peak,
+                         "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
+                         "frac": kernels["qwz_quant_int8"]["frac"],
+                         "traffic": ncu_traffic("qwz_quant_int8", "qwz", w.n)},
+            "kernels": kernels, "gpu_launches": 2 * args.steps}, None
+
+
+def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
+    from weight_communication_gb300 import binding
+    dst = torch.zeros(w.n, dtype=torch.bfloat16, device=dev)
+    pristine = [wl.sr_micro_gradient(w, t, device=dev) for t in range(w.micro_steps)]
+    srcs = [p.clone() for p in pristine]
+    stream = torch.cuda.Stream(dev)
+    names = [f"sr_accumulate[{t}]" for t in range(w.micro_steps)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for t in range(w.micro_steps):
+                binding.sr_accumulate_bf16(dst, srcs[t], w.seed, t, stream)
+            for s, p in zip(srcs, pristine):
+                s.copy_(p)
+        torch.cuda.synchronize(dev)
+        timer = Timer(names, args.steps)
+        barrier(dist)
+        for i in range(args.steps):
+            for t in range(w.micro_steps):
+                timer.mark(i, t)
+                binding.sr_accumulate_bf16(dst, srcs[t], w.seed, t, stream)
+            timer.mark(i, w.micro_steps)
+            for s, p in zip(srcs, pristine):      # refill the sources, untimed
+                s.copy_(p)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+    per = timer.per_kernel_ms()
+    ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
+    peak, kind = measured_peaks()
+    b = w.n * 8
+    launch_ms = statistics.mean(per.values())
+    achieved = b / (launch_ms / 1e3) / 1e9
+    return {"metric": "ZeRO-2 SR accumulate elements/s (8 micro-steps, source zeroed)",
+            "value": w.n * w.micro_steps * ws / (ms / 1e3), "unit": "elements/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded N(0, 1e-4) micro-gradients)",
+            "config": {"workload": w.name, "n": w.n, "micro_steps": w.micro_steps,
+                       "l2": "inputs exceed L2 (1 GB per launch)"},
+            "roofline": {"bound": "hbm", "kernel": "sr_accumulate", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic("sr_accumulate", "sr", w.n)},
+            "kernels": {"sr_accumulate": {"ms": round(launch_ms, 5), "algorithmic_bytes": b,
+                                          "GB/s": round(achieved, 1),
+                                          "frac": round(achieved / peak, 4)}},
+            "gpu_launches": w.micro_steps * args.steps}, None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+def qgz_sample(w: wl.QgzWorkload, fraction: int) -> wl.QgzWorkload:
+    """The workload with each rank's gradient cut to N/fraction elements
+    (same R, G, B, error-feedback parameters and value distribution)."""
+    unit = w.R * w.B
+    n = max(unit, (w.N // fraction) // unit * unit)
+    return w.scaled(n, f"{w.name.split()[0]} sample R={w.R} N={n} B={w.B}")
+
+
+def oracle_qgz_step(orc, w: wl.QgzWorkload, g_u16: np.ndarray, ef: np.ndarray):
+    codes, scales = orc.ef_quant_int4(g_u16, ef, w.N, w.R, w.G, w.B, w.err_scale, w.err_beta)
+    if w.G > 1:
+        c1, s1 = orc.dequant_reduce_requant(codes, scales, w.N, w.R, w.G, w.B)
+        return orc.dequant_reduce(c1, s1, w.N, w.R, w.G, w.B, 1.0, w.out_bf16)
+    return orc.dequant_reduce(codes, scales, w.N, w.R, 1, w.B, 1.0, w.out_bf16)
+
+
+def cpu_baseline_qgz(w: wl.QgzWorkload, steps: int, fraction: int, g_full_example=None):
+    """The oracle, as it stands, timed on this host on a bounded sample."""
+    import oracle
+    orc = oracle.get()
+    sw = qgz_sample(w, fraction)
+    if g_full_example is not None:
+        g = wl.as_u16(g_full_example[:, :sw.N]).ravel().copy()
+    else:
+        g = wl.as_u16(wl.qgz_gradients(sw, 0)).ravel().copy()
+    ef = np.zeros(sw.R * sw.N, np.float32)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_qgz_step(orc, sw, g, ef)
+    dt = time.perf_counter() - t0
+    cores, model = host_cpu()
+    return {"value": sw.R * sw.N * steps / dt, "unit": "elements/s", "cores": 1,
+            "host_cores": cores, "cpu": model, "kind": "oracle",
+            "sample": f"{steps} steps of R={sw.R} ranks x N={sw.N} elements "
+                      f"(1/{fraction} of each rank's gradient; same B, G, LoCo parameters), "
+                      f"{dt:.1f} s single-threaded"}
+
+
+def run_reference(w_name: str, args, ws, rank):
+    """--impl reference: the CPU oracle on the same metric and config."""
+    if ws > 1 and rank != 0:
+        return None
+    import oracle
+    orc = oracle.get()
+    w = wl.QGZ_WORKLOADS.get(w_name)
+    if w is None:
+        return {"impl": "reference", "unavailable": f"no oracle leg for workload {w_name}"}
+    fraction = {"qgz_tiny": 1, "qgz_single_hop": 4, "qgz_hierarchical": 32}[w_name]
+    sw = qgz_sample(w, fraction)
+    batches = [wl.as_u16(wl.qgz_gradients(sw, t)).ravel().copy() for t in range(2)]
+    ef = np.zeros(sw.R * sw.N, np.float32)
+    for i in range(args.warmup):
+        oracle_qgz_step(orc, sw, batches[i % 2], ef)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_qgz_step(orc, sw, batches[i % 2], ef)
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    value = sw.R * sw.N / (ms / 1e3)
+    cores, model = host_cpu()
+    sample = (f"each step R={sw.R} ranks x N={sw.N} elements (1/{fraction} of each rank's "
+              f"gradient of {w.name}; same B, G, LoCo parameters)")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "elements/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded normal gradients with sparse outliers)",
+            "config": {"workload": w.name, "R": w.R, "N": w.N, "G": w.G, "B": w.B,
+                       "err_scale": w.err_scale, "err_beta": w.err_beta,
+                       "parallelism": "single host thread"},
+            "cpu_baseline": {"value": value, "unit": "elements/s", "cores": 1,
+                             "host_cores": cores, "cpu": model, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qgz_single_hop",
+                    choices=["qgz_single_hop", "qgz_tiny", "qgz_hierarchical", "qwz", "sr", "all"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--scale", type=int, default=1,
+                    help="divide each rank's gradient by this (profiling a smaller case)")
+    ap.add_argument("--batches", type=int, default=4,
+                    help="distinct gradient batches cycled through the timed steps")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3                       # at least 3 untimed warm-up steps
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        line = run_reference(args.workload if args.workload in wl.QGZ_WORKLOADS
+                             else "qgz_single_hop", args, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the kernels have no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from weight_communication_gb300 import binding
+    binding.load()                            # fail loudly if the library is missing
+    dist = init_dist(ws, True)
+    names = (["qgz_single_hop", "qgz_tiny", "qgz_hierarchical", "qwz", "sr"]
+             if args.workload == "all" else [args.workload])
+    for name in names:
+        if name in wl.QGZ_WORKLOADS:
+            w = wl.QGZ_WORKLOADS[name]
+            if args.scale > 1:
+                w = qgz_sample(w, args.scale)
+            line, g_example = run_qgz(w, args, dev, dist, ws)
+            if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+                fraction = {"qgz_tiny": 1, "qgz_single_hop": 4, "qgz_hierarchical": 32}[name]
+                line["cpu_baseline"] = cpu_baseline_qgz(w, 6 if name != "qgz_tiny" else 20,
+                                                        fraction, g_example.cpu())
+            del g_example
+        elif name == "qwz":
+            line, _ = run_qwz(wl.QWZ_WEIGHTS, args, dev, dist, ws)
+        else:
+            line, _ = run_sr(wl.SR_ACCUMULATE, args, dev, dist, ws)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,196 @@
+/*
+ * wc.h -- C ABI of the GB300 quantized-gradient communication kernels.
+ *
+ * The hot path of ZeRO++ quantized gradient reduction (qgZ) with LoCo error
+ * feedback, plus qwZ weight quantization and ZeRO-2 stochastic-rounding
+ * gradient accumulation, as sm_103a CUDA kernels.  Several data-parallel
+ * ranks are simulated as slices of one device allocation: the all-to-all of
+ * the real system becomes the address arithmetic by which each reducing
+ * kernel reads its chunks.
+ *
+ * Sources:
+ *   "Merge LoCo with Zero++" (DeepSpeed PR #6730), Overview: error-feedback
+ *     compensation of the 4-bit gradients before communication; review
+ *     thread: two LoCo parameters, one error buffer per parameter.
+ *   "ZeROPlusPlus.md" (notes on ZeRO++), §1.2 ZeRO++: qgZ -- block-based int4
+ *     gradients exchanged by all-to-all in place of reduce-scatter, reduced
+ *     in full precision, intra-node first and inter-node second; qwZ --
+ *     block-based int8 weights for the forward all-gather.
+ *   "Zero 2 #593" (llm.c), review of vector_add and of zero.cuh: bf16
+ *     gradient accumulation summed in fp32 with stochastic rounding, and the
+ *     zeroing of the source fused into the same kernel.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers to memory the caller allocated and owns;
+ *     the library allocates nothing, frees nothing and never synchronizes
+ *     the host.  Every call is asynchronous on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream) and reads/writes its buffers only in
+ *     stream order.
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Every device pointer must be 16-byte aligned (WC_EALIGN otherwise).
+ *   - Buffers must not overlap unless an entry point says so.
+ *   - Inputs must be finite (not checked).
+ *   - Return value: WC_OK, or a negative WC_E* code with nothing launched
+ *     (argument errors) or with the launch failed (WC_ECUDA).  The message
+ *     of the calling thread's last failure is returned by wc_last_error().
+ *   - A size of zero elements is a valid call that launches nothing.
+ *
+ * Arithmetic (shared with the reference definitions): IEEE binary32 with one
+ * rounding per operation (no contraction into fused multiply-adds, no flush
+ * to zero); bf16 results are rounded to nearest even unless stated.
+ */
+#ifndef WC_H
+#define WC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define WC_API __attribute__((visibility("default")))
+#else
+#define WC_API
+#endif
+
+/* status codes */
+#define WC_OK 0
+#define WC_EINVAL (-1)   /* null pointer, bad size or divisibility, bad block */
+#define WC_EALIGN (-2)   /* a pointer is not 16-byte aligned */
+#define WC_ERANGE (-3)   /* a size exceeds what the kernel indexes */
+#define WC_ECUDA (-4)    /* the kernel launch failed; see wc_last_error() */
+
+/* output element types for the reductions */
+#define WC_F32 0
+#define WC_BF16 1
+
+/*
+ * wc_ef_quant_int4 -- error-feedback compensation and int4 quantization of
+ * every simulated rank's gradient (LoCo on qgZ; steps a1-a5).
+ *
+ * For each rank r in [0, R) and element x of its gradient g_r (N elements):
+ *   c = g + s * e                               (fp32; e = ef[r][x])
+ * then per block of B consecutive elements of c, m = max |c|:
+ *   m <  7 * 2^-126: scale = 0, q = 0           (scale would not be normal)
+ *   else:            scale = m / 7, inv = 7 / m, q = clamp(rint(c*inv), -7, 7)
+ * and, when ef != NULL,
+ *   e <- beta * e + (1 - beta) * (c - q * scale)
+ * with 1 - beta formed once in fp32.  ef == NULL quantizes g alone (s and
+ * beta are ignored, no error is stored).
+ *
+ * Send order.  Each rank's N elements are R slices of S = N / R; slice k is
+ * reduced on rank k.  With G groups of L = R / G ranks (rank k = g*L + l) the
+ * codes of slice g'*L + l are written at chunk position l*G + g', so the
+ * chunk bound for local rank l of the first (intra-group) hop is one run of
+ * G*S elements.  G = 1 is the identity (flat all-to-all).
+ *
+ * g      : [R][N] bf16, read.
+ * ef     : [R][N] fp32, read and written in place, gradient order; or NULL.
+ * codes  : [R][N/2] bytes, written, send order.  Code of position p is a
+ *          4-bit two's-complement nibble: low nibble of byte p/2 for even p,
+ *          high nibble for odd p.  Values in [-7, 7].
+ * scales : [R][N/B] fp32, written, send order (one per block of codes).
+ * Requires R >= 1, G >= 1, G | R, R | N, B | N/R, and
+ * B in {32, 64, 128, 256, 512, 1024}.  R*N < 2^32 (WC_ERANGE otherwise).
+ */
+WC_API int wc_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes,
+                            float *scales, int64_t N, int R, int G, int B,
+                            float err_scale, float err_beta, void *stream);
+
+/*
+ * wc_dequant_reduce -- dequantize and reduce in full precision (steps a6-a7,
+ * and a9 for the second hop of the hierarchical reduce).
+ *
+ * Every destination k in [0, R) computes S = N / R outputs
+ *   out[k][i] = out_scale * (d_0 + d_1 + ... + d_{n-1})   (fp32, left to right
+ *                                                          from +0)
+ * where d_j = code * scale of source j, and then stores it as fp32
+ * (out_dtype WC_F32) or rounds it to bf16 (WC_BF16).  out_scale = 1 gives the
+ * sum, 1/R the average.
+ *   G == 1 (flat): the sources are the R ranks' send buffers produced by
+ *     wc_ef_quant_int4 ([R][N/2] codes, [R][N/B] scales); source j of
+ *     destination k is chunk k of rank j (n = R).
+ *   G > 1 (second hop): the sources are the first hop's outputs produced by
+ *     wc_dequant_reduce_requant ([R][G*S/2] codes, [R][G*S/B] scales; unit
+ *     u = g*L + l); destination k = g*L + l adds sub-slice g of units
+ *     (j, l) for j = 0..G-1 (n = G).
+ * out : [R][S] fp32 or bf16, written, destination order (shard k of the
+ *       ZeRO partition is out[k]).
+ * Requires the same sizes as wc_ef_quant_int4.
+ */
+WC_API int wc_dequant_reduce(const uint8_t *codes, const float *scales,
+                             int64_t N, int R, int G, int B, float out_scale,
+                             void *out, int out_dtype, void *stream);
+
+/*
+ * wc_dequant_reduce_requant -- first (intra-group) hop of the hierarchical
+ * reduce, with the partial sums requantized to int4 (step a8).
+ *
+ * Unit (g, l), local rank l of group g, receives from the L ranks g*L + l'
+ * of its group their chunk l (send positions l*G .. l*G+G-1: G sub-slices of
+ * S).  For each sub-slice g' and element i it adds the L dequantized values
+ * in the order l' = 0..L-1 (fp32 from +0), then requantizes each block of B
+ * partial sums with the rule of wc_ef_quant_int4 (no error feedback).
+ * codes, scales : the send buffers of wc_ef_quant_int4 with the same
+ *                 (N, R, G, B), read.
+ * out_codes     : [R][G*S/2] bytes, written; unit u = g*L + l holds its G
+ *                 sub-slices in order g' = 0..G-1 (sub-slice g' is bound for
+ *                 rank g'*L + l).
+ * out_scales    : [R][G*S/B] fp32, written, same order.
+ * Requires the sizes of wc_ef_quant_int4 and G*N < 2^32.  G = 1 is allowed:
+ * it requantizes the flat reduce.
+ */
+WC_API int wc_dequant_reduce_requant(const uint8_t *codes, const float *scales,
+                                     int64_t N, int R, int G, int B,
+                                     uint8_t *out_codes, float *out_scales,
+                                     void *stream);
+
+/*
+ * wc_qwz_quant_int8 -- qwZ block weight quantization (step a10).
+ * Per block of B weights (bf16 widened exactly to fp32), m = max |w|:
+ *   m < 127 * 2^-126: scale = 0, q = 0
+ *   else: scale = m / 127, inv = 127 / m, q = clamp(rint(w * inv), -127, 127)
+ * w : [n] bf16, read.  codes : [n] int8, written.  scales : [n/B] fp32.
+ * Requires B | n and B in {32, 64, ..., 4096} (powers of two).  n < 2^32.
+ */
+WC_API int wc_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
+                             int64_t n, int B, void *stream);
+
+/*
+ * wc_qwz_dequant_int8 -- back to bf16 (step a11): w' = bf16_rn(q * scale).
+ * codes : [n] int8, scales : [n/B] fp32, read.  w_out : [n] bf16, written.
+ * Same size rules as wc_qwz_quant_int8.
+ */
+WC_API int wc_qwz_dequant_int8(const int8_t *codes, const float *scales,
+                               uint16_t *w_out, int64_t n, int B, void *stream);
+
+/*
+ * wc_sr_accumulate_bf16 -- ZeRO-2 gradient accumulation with stochastic
+ * rounding and the source zeroed in the same kernel (step a12).
+ * For i in [0, n):
+ *   x = f32(dst[i]) + f32(src[i])                       (fp32)
+ *   r = mix(key ^ i) & 0xFFFF,  key = mix(mix(seed) ^ step),
+ *       mix(z) = fmix32(z + 0x9E3779B9)  (MurmurHash3's 32-bit finalizer)
+ *   dst[i] = upper half of (bits(x) + r)                 (rounds the
+ *            magnitude up with probability (low 16 bits of x) / 65536)
+ *   src[i] = 0
+ * Unbiased: the mean over r is exactly x.  Infinities pass through; sums
+ * within one bf16 step of the largest finite value may round to infinity.
+ * dst, src : [n] bf16, read and written in place; they must not overlap.
+ * Requires n < 2^32 (the index is 32-bit).
+ */
+WC_API int wc_sr_accumulate_bf16(uint16_t *dst, uint16_t *src, int64_t n,
+                                 uint32_t seed, uint32_t step, void *stream);
+
+/* Message describing the calling thread's last failed call ("" if none). */
+WC_API const char *wc_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+WC_API int wc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WC_H */

@@ -1,0 +1,220 @@
+"""GPU parity of the qgZ kernels (through the C ABI) against the CPU oracle.
+
+Inputs are seeded bf16 gradients (normal with sparse outliers, as the
+Llama-2 layer workloads) plus hand-made edge blocks; both sides get the same
+bytes.  Sizes span many warp tiles with ragged tails, every supported block
+size, flat and grouped send orders, with and without error feedback, and the
+multi-step error-feedback recurrence.  Full-size runs of the three qgZ
+workloads are in test_parity_fullsize.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (assert_bf16_parity, assert_bits_equal, assert_f32_parity, deq_magnitude,
+                      dev, to_dev, to_host)
+from weight_communication_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+ORC = oracle.get()
+
+
+def edge_gradients(R: int, N: int, B: int, seed: int) -> np.ndarray:
+    """[R*N] bf16 bits: seeded values with outliers, with some blocks replaced
+    by edge cases -- all zero, signed zeros, subnormal, at the zero-block
+    threshold 7*2^-126 and just below it, exact rounding ties, huge values."""
+    g = wl.as_u16(wl.draw_bf16(R * N, 1e-3, seed, outlier_frac=1e-3, outlier_mult=100.0)).copy()
+    nb = R * N // B
+    rng = np.random.default_rng(seed)
+    tiny = np.float32(np.finfo(np.float32).tiny)
+    specials = [
+        np.zeros(B, np.float32),
+        np.where(np.arange(B) % 2 == 0, np.float32(0.0), np.float32(-0.0)),
+        np.float32(1e-39) * rng.standard_normal(B).astype(np.float32),       # subnormal
+        np.concatenate([[np.float32(7) * tiny], rng.uniform(-1, 1, B - 1).astype(np.float32) * tiny]),
+        np.concatenate([[np.float32(6) * tiny], np.zeros(B - 1, np.float32)]),
+        np.concatenate([[np.float32(7.0)], (np.arange(B - 1) % 15 - 7 + 0.5).astype(np.float32)]),
+        np.concatenate([[np.float32(-7.0)], (np.arange(B - 1) % 13 - 6.5).astype(np.float32)]),
+        rng.standard_normal(B).astype(np.float32) * np.float32(1e30),
+    ]
+    picks = rng.choice(nb, size=min(nb, 3 * len(specials)), replace=False)
+    for j, b in enumerate(picks):
+        blk = torch.from_numpy(specials[j % len(specials)].astype(np.float32)).to(torch.bfloat16)
+        g[b * B:(b + 1) * B] = wl.as_u16(blk)
+    return g
+
+
+def gpu_ef_quant(g_u16, ef, N, R, G, B, s, beta, dev):
+    gd = to_dev(g_u16, dev)
+    efd = to_dev(ef, dev) if ef is not None else None
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    binding.ef_quant_int4(gd, efd, codes, scales, N, R, G, B, s, beta)
+    torch.cuda.synchronize()
+    return to_host(codes), to_host(scales), (to_host(efd) if efd is not None else None)
+
+
+CASES = [
+    # R, N, G, B, s, beta, with_ef
+    (4, 4 * 256 * 37, 1, 256, 1.0, 0.0, True),
+    (8, 8 * 256 * 11, 1, 256, 1.0, 0.5, True),
+    (3, 3 * 512 * 7, 1, 512, 1.0, 0.5, True),
+    (16, 16 * 512 * 3, 2, 512, 1.0, 0.5, True),
+    (6, 6 * 1024 * 2, 3, 1024, 0.75, 0.25, True),
+    (8, 8 * 128 * 9, 4, 128, 2.0, 0.5, True),
+    (4, 4 * 64 * 13, 2, 64, 1.0, 0.5, True),       # 2 blocks per warp tile, ragged tail
+    (2, 2 * 32 * 7, 1, 32, 1.0, 0.0, True),        # 4 blocks per warp tile, ragged tail
+    (1, 32, 1, 32, 1.0, 0.5, True),                # a single block, partial warp tile
+    (5, 5 * 256 * 3, 5, 256, 1.0, 0.0, False),
+    (12, 12 * 64 * 5, 4, 64, 1.0, 0.0, False),
+]
+
+
+@pytest.mark.parametrize("R,N,G,B,s,beta,with_ef", CASES)
+def test_ef_quant_int4_parity(dev, R, N, G, B, s, beta, with_ef):
+    g = edge_gradients(R, N, B, seed=R * 1000 + B)
+    rng = np.random.default_rng(B)
+    ef0 = (rng.standard_normal(R * N) * 1e-4).astype(np.float32) if with_ef else None
+    gc, gs, ge = gpu_ef_quant(g, ef0, N, R, G, B, s, beta, dev)
+    ef_cpu = ef0.copy() if with_ef else None
+    cc, cs = ORC.ef_quant_int4(g, ef_cpu, N, R, G, B, s, beta)
+    assert_bits_equal(gc, cc, "codes")
+    assert_bits_equal(gs, cs, "scales")
+    if with_ef:
+        gf = (g.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ref = np.abs(gf) + abs(s) * np.abs(ef0) + np.abs(ef_cpu)
+        assert_f32_parity(ge, ef_cpu, ref, "error feedback")
+
+
+def test_error_feedback_recurrence_tiny_workload(dev):
+    """Three steps of the 4-rank, 1M-element workload with plain error
+    feedback: each side carries its own error buffer from step to step."""
+    w = wl.QGZ_TINY
+    ef_cpu = np.zeros(w.R * w.N, np.float32)
+    efd = torch.zeros(w.R * w.N, dtype=torch.float32, device=dev)
+    codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+    out = torch.empty(w.N, dtype=torch.float32, device=dev)
+    for t in range(w.steps):
+        gd = wl.qgz_gradients(w, t, device=dev)
+        g = to_host(gd).ravel()
+        binding.ef_quant_int4(gd.view(-1), efd, codes, scales, w.N, w.R, w.G, w.B,
+                              w.err_scale, w.err_beta)
+        binding.dequant_reduce(codes, scales, out, w.N, w.R, 1, w.B)
+        torch.cuda.synchronize()
+        cc, cs = ORC.ef_quant_int4(g, ef_cpu, w.N, w.R, w.G, w.B, w.err_scale, w.err_beta)
+        co = ORC.dequant_reduce(cc, cs, w.N, w.R, 1, w.B)
+        assert_bits_equal(to_host(codes), cc, f"codes step {t}")
+        assert_bits_equal(to_host(scales), cs, f"scales step {t}")
+        assert_f32_parity(to_host(efd), ef_cpu, np.abs(ef_cpu) + 1e-3, f"ef step {t}")
+        ref = deq_magnitude(cc, cs, w.B).reshape(w.R, w.N).sum(0)
+        assert_f32_parity(to_host(out), co, ref, f"reduced step {t}")
+
+
+REDUCE_CASES = [
+    # R, N, B, out_bf16, out_scale
+    (4, 4 * 256 * 19, 256, False, 1.0),
+    (8, 8 * 256 * 5, 256, False, 0.125),
+    (8, 8 * 256 * 5, 256, True, 1.0),
+    (1, 256 * 9, 256, False, 1.0),
+    (3, 3 * 32 * 11, 32, False, 1.0),
+    (11, 11 * 64 * 3, 64, True, 1.0 / 11),
+    (20, 20 * 128 * 2, 128, False, 1.0),          # more sources than one load batch
+    (16, 16 * 1024, 1024, False, 1.0),
+]
+
+
+@pytest.mark.parametrize("R,N,B,out_bf16,out_scale", REDUCE_CASES)
+def test_flat_dequant_reduce_parity(dev, R, N, B, out_bf16, out_scale):
+    g = edge_gradients(R, N, B, seed=7 * R + B)
+    cc, cs = ORC.ef_quant_int4(g, None, N, R, 1, B, 1.0, 0.0)
+    out = torch.empty(N, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
+    binding.dequant_reduce(to_dev(cc, dev), to_dev(cs, dev), out, N, R, 1, B, out_scale)
+    torch.cuda.synchronize()
+    want = ORC.dequant_reduce(cc, cs, N, R, 1, B, out_scale, out_bf16)
+    if out_bf16:
+        assert_bf16_parity(to_host(out), want, "bf16 shards")
+    else:
+        ref = deq_magnitude(cc, cs, B).reshape(R, N).sum(0) * abs(out_scale)
+        assert_f32_parity(to_host(out), want, ref, "fp32 shards")
+
+
+HIER_CASES = [
+    # R, G, B, shards of S = B * k
+    (16, 2, 512, 3),
+    (8, 4, 128, 5),
+    (12, 3, 64, 7),
+    (8, 2, 32, 9),
+    (8, 1, 256, 4),        # one group: first hop requantizes the flat reduce
+    (4, 4, 1024, 1),       # one rank per group: first hop is a requantization
+]
+
+
+@pytest.mark.parametrize("R,G,B,k", HIER_CASES)
+def test_hierarchical_parity(dev, R, G, B, k):
+    N = R * B * k
+    g = edge_gradients(R, N, B, seed=31 * R + G)
+    ef0 = np.zeros(R * N, np.float32)
+    # quantization with error feedback on the first hop
+    gc, gs, ge = gpu_ef_quant(g, ef0.copy(), N, R, G, B, 1.0, 0.5, dev)
+    ef_cpu = ef0.copy()
+    cc, cs = ORC.ef_quant_int4(g, ef_cpu, N, R, G, B, 1.0, 0.5)
+    assert_bits_equal(gc, cc, "codes")
+    assert_bits_equal(gs, cs, "scales")
+    # hop 1 from the oracle's codes
+    c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    binding.dequant_reduce_requant(to_dev(cc, dev), to_dev(cs, dev), c1, s1, N, R, G, B)
+    torch.cuda.synchronize()
+    oc1, os1 = ORC.dequant_reduce_requant(cc, cs, N, R, G, B)
+    assert_bits_equal(to_host(c1), oc1, "hop-1 codes")
+    assert_bits_equal(to_host(s1), os1, "hop-1 scales")
+    # hop 2 from the oracle's hop-1 output
+    if G > 1:
+        out = torch.empty(N, dtype=torch.bfloat16, device=dev)
+        binding.dequant_reduce(to_dev(oc1, dev), to_dev(os1, dev), out, N, R, G, B)
+        torch.cuda.synchronize()
+        want = ORC.dequant_reduce(oc1, os1, N, R, G, B, 1.0, True)
+        assert_bf16_parity(to_host(out), want, "hop-2 shards")
+        outf = torch.empty(N, dtype=torch.float32, device=dev)
+        binding.dequant_reduce(to_dev(oc1, dev), to_dev(os1, dev), outf, N, R, G, B, 0.5)
+        torch.cuda.synchronize()
+        wantf = ORC.dequant_reduce(oc1, os1, N, R, G, B, 0.5, False)
+        assert_bits_equal(to_host(outf), wantf, "hop-2 fp32 shards")
+
+
+def test_zero_size_calls_launch_nothing(dev):
+    sentinel = torch.full((64,), 7, dtype=torch.uint8, device=dev)
+    binding.ef_quant_int4(torch.empty(0, dtype=torch.bfloat16, device=dev), None,
+                          torch.empty(0, dtype=torch.uint8, device=dev),
+                          torch.empty(0, dtype=torch.float32, device=dev), 0, 4, 1, 256)
+    torch.cuda.synchronize()
+    assert bool((sentinel == 7).all())
+
+
+def test_outputs_stay_inside_their_buffers(dev):
+    """Guard regions around every output stay untouched (ragged sizes)."""
+    R, G, B = 6, 3, 64
+    N = R * B * 5
+    g = edge_gradients(R, N, B, seed=99)
+    pad = 4096
+    gd = to_dev(g, dev)
+    efd = torch.zeros(R * N + 2 * pad, dtype=torch.float32, device=dev).fill_(13.0)
+    efd[pad:pad + R * N] = 0.0
+    codes = torch.full((R * N // 2 + 2 * pad,), 0xA5, dtype=torch.uint8, device=dev)
+    scales = torch.full((R * N // B + 2 * pad,), -5.0, dtype=torch.float32, device=dev)
+    binding.ef_quant_int4(gd, efd[pad:pad + R * N], codes[pad:pad + R * N // 2],
+                          scales[pad:pad + R * N // B], N, R, G, B, 1.0, 0.5)
+    c1 = torch.full((G * N // 2 + 2 * pad,), 0x5A, dtype=torch.uint8, device=dev)
+    s1 = torch.full((G * N // B + 2 * pad,), -9.0, dtype=torch.float32, device=dev)
+    binding.dequant_reduce_requant(codes[pad:pad + R * N // 2], scales[pad:pad + R * N // B],
+                                   c1[pad:pad + G * N // 2], s1[pad:pad + G * N // B], N, R, G, B)
+    out = torch.full((N + 2 * pad,), -1.0, dtype=torch.float32, device=dev)
+    binding.dequant_reduce(c1[pad:pad + G * N // 2], s1[pad:pad + G * N // B],
+                           out[pad:pad + N], N, R, G, B)
+    torch.cuda.synchronize()
+    for t, fill, n in ((efd, 13.0, R * N), (codes, 0xA5, R * N // 2), (scales, -5.0, R * N // B),
+                       (c1, 0x5A, G * N // 2), (s1, -9.0, G * N // B), (out, -1.0, N)):
+        assert bool((t[:pad] == fill).all()) and bool((t[pad + n:] == fill).all())

@@ -1,0 +1,175 @@
+"""ctypes binding of libwc.so (include/wc.h): argument marshalling only.
+
+Every function takes torch CUDA tensors, checks dtype, device, contiguity and
+sizes, and calls the entry point of the same name on the tensors' current
+stream.  All arithmetic happens in the CUDA kernels; there is no CPU or
+PyTorch fallback -- if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+from . import build as _build
+
+WC_OK, WC_EINVAL, WC_EALIGN, WC_ERANGE, WC_ECUDA = 0, -1, -2, -3, -4
+WC_F32, WC_BF16 = 0, 1
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_F = ctypes.c_float
+_U32 = ctypes.c_uint32
+
+# name -> argtypes (all return int except the two informational calls)
+SIGNATURES = {
+    "wc_ef_quant_int4": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
+    "wc_dequant_reduce": [_P, _P, _I64, _I, _I, _I, _F, _P, _I, _P],
+    "wc_dequant_reduce_requant": [_P, _P, _I64, _I, _I, _I, _P, _P, _P],
+    "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
+    "wc_qwz_dequant_int8": [_P, _P, _P, _I64, _I, _P],
+    "wc_sr_accumulate_bf16": [_P, _P, _I64, _U32, _U32, _P],
+    "wc_last_error": [],
+    "wc_version": [],
+}
+
+
+class WcError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed with status {code}: {msg}")
+        self.code = code
+
+
+_lib: ctypes.CDLL | None = None
+
+
+def library_path() -> Path:
+    return _build.LIB
+
+
+def load(path: str | Path | None = None) -> ctypes.CDLL:
+    """Load libwc.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = Path(path) if path is not None else library_path()
+    if not p.exists():
+        raise RuntimeError(f"CUDA library {p} is missing: build it with "
+                           "`python -m weight_communication_gb300.build`")
+    lib = ctypes.CDLL(str(p))
+    for name, args in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "wc_last_error" else ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load().wc_last_error().decode()
+
+
+def version() -> int:
+    return load().wc_version()
+
+
+def _call(name: str, *args) -> None:
+    lib = load()
+    rc = getattr(lib, name)(*args)
+    if rc != WC_OK:
+        raise WcError(name, rc, lib.wc_last_error().decode())
+
+
+def _stream(t: torch.Tensor, stream: torch.cuda.Stream | None):
+    s = stream if stream is not None else torch.cuda.current_stream(t.device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor | None, name: str, dtype: torch.dtype, numel: int, device=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() != numel:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def ef_quant_int4(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor,
+                  scales: torch.Tensor, N: int, R: int, G: int, B: int,
+                  err_scale: float = 1.0, err_beta: float = 0.0, stream=None) -> None:
+    """wc_ef_quant_int4: g bf16 [R*N], ef fp32 [R*N] (in place) or None,
+    codes uint8 [R*N/2], scales fp32 [R*N/B] -- all written in send order."""
+    d = g.device
+    _call("wc_ef_quant_int4", _dev(g, "g", torch.bfloat16, R * N, d),
+          _dev(ef, "ef", torch.float32, R * N, d), _dev(codes, "codes", torch.uint8, R * N // 2, d),
+          _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
+          _stream(g, stream))
+
+
+def dequant_reduce(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor, N: int,
+                   R: int, G: int, B: int, out_scale: float = 1.0, stream=None) -> None:
+    """wc_dequant_reduce: out fp32 or bf16 [R*S] = [N] in destination order.
+    G == 1: codes/scales are the ranks' send buffers ([R*N/2], [R*N/B]);
+    G > 1: they are the first hop's outputs ([G*N/2], [G*N/B])."""
+    d = codes.device
+    span = N * (G if G > 1 else R)
+    if out.dtype == torch.float32:
+        od = WC_F32
+    elif out.dtype == torch.bfloat16:
+        od = WC_BF16
+    else:
+        raise TypeError("out must be float32 or bfloat16")
+    _call("wc_dequant_reduce", _dev(codes, "codes", torch.uint8, span // 2, d),
+          _dev(scales, "scales", torch.float32, span // B, d), N, R, G, B, out_scale,
+          _dev(out, "out", out.dtype, N, d), od, _stream(codes, stream))
+
+
+def dequant_reduce_requant(codes: torch.Tensor, scales: torch.Tensor, out_codes: torch.Tensor,
+                           out_scales: torch.Tensor, N: int, R: int, G: int, B: int,
+                           stream=None) -> None:
+    """wc_dequant_reduce_requant: first hop; out_codes uint8 [G*N/2],
+    out_scales fp32 [G*N/B] (unit u = g*L + l holds G*S values)."""
+    d = codes.device
+    _call("wc_dequant_reduce_requant", _dev(codes, "codes", torch.uint8, R * N // 2, d),
+          _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B,
+          _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
+          _dev(out_scales, "out_scales", torch.float32, G * N // B, d), _stream(codes, stream))
+
+
+def qwz_quant_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, B: int,
+                   stream=None) -> None:
+    n = w.numel()
+    d = w.device
+    _call("wc_qwz_quant_int8", _dev(w, "w", torch.bfloat16, n, d),
+          _dev(codes, "codes", torch.int8, n, d), _dev(scales, "scales", torch.float32, n // B, d),
+          n, B, _stream(w, stream))
+
+
+def qwz_dequant_int8(codes: torch.Tensor, scales: torch.Tensor, w_out: torch.Tensor, B: int,
+                     stream=None) -> None:
+    n = codes.numel()
+    d = codes.device
+    _call("wc_qwz_dequant_int8", _dev(codes, "codes", torch.int8, n, d),
+          _dev(scales, "scales", torch.float32, n // B, d),
+          _dev(w_out, "w_out", torch.bfloat16, n, d), n, B, _stream(codes, stream))
+
+
+def sr_accumulate_bf16(dst: torch.Tensor, src: torch.Tensor, seed: int, step: int,
+                       stream=None) -> None:
+    """dst <- SR_bf16(dst + src) in place; src <- 0."""
+    n = dst.numel()
+    d = dst.device
+    _call("wc_sr_accumulate_bf16", _dev(dst, "dst", torch.bfloat16, n, d),
+          _dev(src, "src", torch.bfloat16, n, d), n, seed & 0xFFFFFFFF, step & 0xFFFFFFFF,
+          _stream(dst, stream))

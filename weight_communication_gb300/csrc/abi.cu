@@ -1,0 +1,178 @@
+// abi.cu -- the extern "C" entry points declared in include/wc.h: argument
+// validation on the host, then exactly one kernel launch per call.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/wc.h"
+#include "wc_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int from_cuda(cudaError_t err, const char *what) {
+    if (err == cudaSuccess) return WC_OK;
+    return fail(WC_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2_in(int64_t b, int64_t lo, int64_t hi) {
+    return b >= lo && b <= hi && (b & (b - 1)) == 0;
+}
+
+// Validates the sizes shared by the qgZ entry points and fills `geo`.
+// Returns WC_OK, or an error code with the message set.
+int qgz_geometry(const char *fn, int64_t N, int R, int G, int B, wc::QgzGeometry *geo) {
+    if (N < 0) return fail(WC_EINVAL, "%s: N = %lld is negative", fn, (long long)N);
+    if (R < 1 || G < 1) return fail(WC_EINVAL, "%s: need R >= 1 and G >= 1 (R=%d, G=%d)", fn, R, G);
+    if (R % G) return fail(WC_EINVAL, "%s: G=%d does not divide R=%d", fn, G, R);
+    if (!pow2_in(B, 32, 1024))
+        return fail(WC_EINVAL, "%s: block B=%d must be a power of two in [32, 1024]", fn, B);
+    if (N % R) return fail(WC_EINVAL, "%s: R=%d does not divide N=%lld", fn, R, (long long)N);
+    const int64_t S = N / R;
+    if (S % B) return fail(WC_EINVAL, "%s: B=%d does not divide the shard N/R=%lld", fn, B, (long long)S);
+    if (N >= (int64_t(1) << 32) || N * (int64_t)R >= (int64_t(1) << 32))
+        return fail(WC_ERANGE, "%s: R*N = %lld must be below 2^32", fn, (long long)(N * R));
+    geo->N = uint32_t(N);
+    geo->S = uint32_t(S);
+    geo->R = uint32_t(R);
+    geo->G = uint32_t(G);
+    geo->L = uint32_t(R / G);
+    geo->blocks_per_rank = uint32_t(N / B);
+    geo->total = uint32_t(N * R);
+    return WC_OK;
+}
+
+#define WC_REQUIRE_PTR(fn, p)                                                        \
+    do {                                                                             \
+        if ((p) == nullptr) return fail(WC_EINVAL, "%s: %s is NULL", fn, #p);        \
+        if (!aligned16(p)) return fail(WC_EALIGN, "%s: %s is not 16-byte aligned", fn, #p); \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+WC_API const char *wc_last_error(void) { return g_last_error; }
+
+WC_API int wc_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+WC_API int wc_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                            int64_t N, int R, int G, int B, float err_scale, float err_beta,
+                            void *stream) {
+    static const char *fn = "wc_ef_quant_int4";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, g);
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
+    return from_cuda(wc::launch_ef_quant_int4(g, ef, codes, scales, geo, B, err_scale, err_beta,
+                                              static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_dequant_reduce(const uint8_t *codes, const float *scales, int64_t N, int R,
+                             int G, int B, float out_scale, void *out, int out_dtype,
+                             void *stream) {
+    static const char *fn = "wc_dequant_reduce";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (out_dtype != WC_F32 && out_dtype != WC_BF16)
+        return fail(WC_EINVAL, "%s: out_dtype %d is neither WC_F32 nor WC_BF16", fn, out_dtype);
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    WC_REQUIRE_PTR(fn, out);
+    return from_cuda(wc::launch_dequant_reduce(codes, scales, geo, B, out_scale, out,
+                                               out_dtype == WC_BF16,
+                                               static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_dequant_reduce_requant(const uint8_t *codes, const float *scales, int64_t N,
+                                     int R, int G, int B, uint8_t *out_codes,
+                                     float *out_scales, void *stream) {
+    static const char *fn = "wc_dequant_reduce_requant";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (N * (int64_t)G >= (int64_t(1) << 32))
+        return fail(WC_ERANGE, "%s: G*N must be below 2^32", fn);
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    WC_REQUIRE_PTR(fn, out_codes);
+    WC_REQUIRE_PTR(fn, out_scales);
+    return from_cuda(wc::launch_dequant_reduce_requant(codes, scales, out_codes, out_scales, geo,
+                                                       B, static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+static int qwz_sizes(const char *fn, int64_t n, int B) {
+    if (n < 0) return fail(WC_EINVAL, "%s: n = %lld is negative", fn, (long long)n);
+    if (!pow2_in(B, 32, 4096))
+        return fail(WC_EINVAL, "%s: block B=%d must be a power of two in [32, 4096]", fn, B);
+    if (n % B) return fail(WC_EINVAL, "%s: B=%d does not divide n=%lld", fn, B, (long long)n);
+    if (n >= (int64_t(1) << 32)) return fail(WC_ERANGE, "%s: n must be below 2^32", fn);
+    return WC_OK;
+}
+
+WC_API int wc_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, int64_t n, int B,
+                             void *stream) {
+    static const char *fn = "wc_qwz_quant_int8";
+    int rc = qwz_sizes(fn, n, B);
+    if (rc != WC_OK) return rc;
+    if (n == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, w);
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    return from_cuda(wc::launch_qwz_quant_int8(w, codes, scales, uint32_t(n), B,
+                                               static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_qwz_dequant_int8(const int8_t *codes, const float *scales, uint16_t *w_out,
+                               int64_t n, int B, void *stream) {
+    static const char *fn = "wc_qwz_dequant_int8";
+    int rc = qwz_sizes(fn, n, B);
+    if (rc != WC_OK) return rc;
+    if (n == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    WC_REQUIRE_PTR(fn, w_out);
+    return from_cuda(wc::launch_qwz_dequant_int8(codes, scales, w_out, uint32_t(n), B,
+                                                 static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_sr_accumulate_bf16(uint16_t *dst, uint16_t *src, int64_t n, uint32_t seed,
+                                 uint32_t step, void *stream) {
+    static const char *fn = "wc_sr_accumulate_bf16";
+    if (n < 0) return fail(WC_EINVAL, "%s: n = %lld is negative", fn, (long long)n);
+    if (n >= (int64_t(1) << 32)) return fail(WC_ERANGE, "%s: n must be below 2^32", fn);
+    if (n == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, dst);
+    WC_REQUIRE_PTR(fn, src);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst), b = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t bytes = uintptr_t(n) * 2u;
+    if (a < b + bytes && b < a + bytes) return fail(WC_EINVAL, "%s: dst and src overlap", fn);
+    return from_cuda(wc::launch_sr_accumulate(dst, src, uint32_t(n), seed, step,
+                                              static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+}  // extern "C"

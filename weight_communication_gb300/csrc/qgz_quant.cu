@@ -1,0 +1,262 @@
+// qgz_quant.cu -- kernels that produce int4 codes:
+//   * error-feedback compensation + int4 block quantization of every rank's
+//     gradient, written in all-to-all send order (LoCo on qgZ);
+//   * the first hop of the hierarchical reduce: dequantize the L chunks a
+//     unit receives from its group, add them in fp32, requantize to int4.
+//
+// "Merge LoCo with Zero++" (DeepSpeed PR #6730), Overview: the 4-bit
+// gradients are compensated with an error-feedback buffer before they are
+// communicated.  "ZeROPlusPlus.md", §1.2 ZeRO++ (quantized gradient
+// communication): block-based int4 quantization, all-to-all in place of the
+// reduce-scatter, reduction in full precision, intra-node before inter-node,
+// with kernel fusion.
+//
+// Both kernels are HBM-bound streams (about 10.5 bytes per gradient element
+// for the first, 4.6 per output element for the second).  One warp owns one
+// quantization block (or, for blocks smaller than the warp tile, each aligned
+// group of lanes owns one block), so the absmax is a warp-shuffle reduction
+// and codes, scales and the error update are produced in the same pass that
+// loads the block -- no second read, no shared memory, no block barrier.
+#include "wc_device.cuh"
+#include "wc_internal.h"
+
+namespace wc {
+
+// ---------------------------------------------------------------------------
+// EF compensation + int4 quantization
+// ---------------------------------------------------------------------------
+//
+// Lane layout: a warp tile is T = max(B, 128) consecutive gradient elements;
+// lane t holds elements 128*k + 4*t + j (k < T/128, j < 4).  Every access is
+// then fully coalesced: 8-byte bf16 loads (256 B per warp instruction),
+// 16-byte fp32 error loads and stores (512 B), 2-byte code stores (64 B).
+template <int B, bool HAS_EF>
+__global__ void __launch_bounds__(256)
+ef_quant_int4_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
+                     uint8_t *__restrict__ codes, float *__restrict__ scales,
+                     QgzGeometry geo, float s, float beta, float one_minus_beta) {
+    constexpr int T = B >= 128 ? B : 128;
+    constexpr int K = T / 128;
+    constexpr int LPB = B >= 128 ? 32 : B / 4;  // lanes per block
+    const int lane = threadIdx.x & (kWarp - 1);
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    // Warps past the end (the grid is rounded up to whole CTAs) leave at once;
+    // the comparison is 64-bit so a tile start cannot wrap around 2^32.
+    if (uint64_t(warp) * T >= geo.total) return;
+    const uint32_t tile0 = warp * uint32_t(T);
+
+    // Block owned by this lane and its position in send order.
+    const uint32_t first = tile0 + (B >= 128 ? 0u : 4u * lane);
+    const bool active = first < geo.total;
+    const uint32_t blk = first / B;
+    const uint32_t r = blk / geo.blocks_per_rank;
+    const uint32_t x0 = (blk - r * geo.blocks_per_rank) * B;  // element in rank
+    const uint32_t slice = x0 / geo.S;
+    const uint32_t off = x0 - slice * geo.S;
+    const uint32_t gq = slice / geo.L;
+    const uint32_t l = slice - gq * geo.L;
+    const uint32_t out0 = r * geo.N + (l * geo.G + gq) * geo.S + off;  // code position
+
+    float c[K][4];
+    float e[K][4];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const uint32_t x = tile0 + 128u * k + 4u * lane;
+        uint2 gv = make_uint2(0u, 0u);
+        float4 ev = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active) {
+            gv = ld_stream_u2(g + x);
+            if (HAS_EF) ev = ld_stream_f4(ef + x);
+        }
+        const float gf[4] = {bf16_bits_to_f32(gv.x & 0xFFFFu), bf16_bits_to_f32(gv.x >> 16),
+                             bf16_bits_to_f32(gv.y & 0xFFFFu), bf16_bits_to_f32(gv.y >> 16)};
+        e[k][0] = ev.x; e[k][1] = ev.y; e[k][2] = ev.z; e[k][3] = ev.w;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            c[k][j] = HAS_EF ? __fadd_rn(gf[j], __fmul_rn(s, e[k][j])) : gf[j];
+    }
+
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = fmaxf(m, fabsf(c[k][j]));
+    m = group_max<LPB>(m);
+    const BlockScale bs = block_scale<7>(m);
+    if (!active) return;
+
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        int q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) q[j] = quant_code<7>(c[k][j], bs);
+        const uint32_t packed = (uint32_t(q[0]) & 15u) | ((uint32_t(q[1]) & 15u) << 4) |
+                                ((uint32_t(q[2]) & 15u) << 8) | ((uint32_t(q[3]) & 15u) << 12);
+        const uint32_t in_blk = B >= 128 ? 128u * k + 4u * lane : (4u * lane) % B;
+        const uint32_t pos = out0 + in_blk;
+        __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2), (unsigned short)packed);
+        if (HAS_EF) {
+            float4 ev;
+            float *o = &ev.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float d = dequant(q[j], bs.scale);
+                o[j] = __fadd_rn(__fmul_rn(beta, e[k][j]),
+                                 __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));
+            }
+            const uint32_t x = tile0 + 128u * k + 4u * lane;
+            __stcs(reinterpret_cast<float4 *>(ef + x), ev);
+        }
+    }
+    if ((lane & (LPB - 1)) == 0) __stcs(scales + out0 / B, bs.scale);
+}
+
+template <int B>
+static cudaError_t launch_ef_quant_b(const uint16_t *g, float *ef, uint8_t *codes,
+                                     float *scales, const QgzGeometry &geo, float s,
+                                     float beta, cudaStream_t stream) {
+    constexpr int T = B >= 128 ? B : 128;
+    const uint32_t tiles = (geo.total + T - 1) / T;
+    const uint32_t threads = 256;
+    const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
+    const float omb = 1.0f - beta;
+    if (ef)
+        ef_quant_int4_kernel<B, true><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
+                                                                     s, beta, omb);
+    else
+        ef_quant_int4_kernel<B, false><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
+                                                                      s, beta, omb);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                                 const QgzGeometry &geo, int B, float s, float beta,
+                                 cudaStream_t stream) {
+    switch (B) {
+        case 32: return launch_ef_quant_b<32>(g, ef, codes, scales, geo, s, beta, stream);
+        case 64: return launch_ef_quant_b<64>(g, ef, codes, scales, geo, s, beta, stream);
+        case 128: return launch_ef_quant_b<128>(g, ef, codes, scales, geo, s, beta, stream);
+        case 256: return launch_ef_quant_b<256>(g, ef, codes, scales, geo, s, beta, stream);
+        case 512: return launch_ef_quant_b<512>(g, ef, codes, scales, geo, s, beta, stream);
+        case 1024: return launch_ef_quant_b<1024>(g, ef, codes, scales, geo, s, beta, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// First hop: dequantize L chunks, reduce in fp32, requantize to int4
+// ---------------------------------------------------------------------------
+//
+// Output element o (over all R units, G*S each) belongs to unit u = g*L + l,
+// sub-slice g' and offset i; its inputs are the codes at position
+// (g*L + l')*N + (l*G + g')*S + i for l' = 0..L-1.  Lane layout: warp tile
+// T = max(B, 256) outputs, lane t holds outputs 256*k + 8*t + j, i.e. one
+// 32-bit word of codes per source and per k: 128-byte coalesced loads and
+// stores per warp instruction.
+template <int B>
+__global__ void __launch_bounds__(256)
+dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
+                              const float *__restrict__ scales,
+                              uint8_t *__restrict__ out_codes,
+                              float *__restrict__ out_scales, QgzGeometry geo) {
+    constexpr int T = B >= 256 ? B : 256;
+    constexpr int K = T / 256;
+    constexpr int LPB = B >= 256 ? 32 : B / 8;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    const uint32_t total_out = geo.G * geo.N;  // R units * G*S
+    if (uint64_t(warp) * T >= total_out) return;
+    const uint32_t tile0 = warp * uint32_t(T);
+
+    const uint32_t unit_len = geo.G * geo.S;
+    float acc[K][8];
+    bool active[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const uint32_t o = tile0 + 256u * k + 8u * lane;
+        active[k] = o < total_out;
+        const uint32_t oo = active[k] ? o : tile0;
+        const uint32_t u = oo / unit_len;
+        const uint32_t rem = oo - u * unit_len;
+        const uint32_t gq = rem / geo.S;
+        const uint32_t i = rem - gq * geo.S;
+        const uint32_t grp = u / geo.L;
+        const uint32_t l = u - grp * geo.L;
+        const uint32_t base = (l * geo.G + gq) * geo.S + i;  // within a rank
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[k][j] = 0.0f;
+        if (!active[k]) continue;
+        // Loads for every source first, then the adds in source order.
+        for (uint32_t l0 = 0; l0 < geo.L; l0 += 8) {
+            uint32_t w[8];
+            float sc[8];
+            const uint32_t nb = min(8u, geo.L - l0);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t < nb) {
+                    const uint32_t pos = (grp * geo.L + l0 + t) * geo.N + base;
+                    w[t] = __ldg(reinterpret_cast<const uint32_t *>(codes + pos / 2));
+                    sc[t] = __ldg(scales + pos / B);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t < nb) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        acc[k][j] = __fadd_rn(acc[k][j], dequant(nibble(w[t], j), sc[t]));
+                }
+            }
+        }
+    }
+
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(acc[k][j]));
+    m = group_max<LPB>(m);
+    const BlockScale bs = block_scale<7>(m);
+
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (!active[k]) continue;
+        const uint32_t o = tile0 + 256u * k + 8u * lane;
+        uint32_t packed = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            packed |= (uint32_t(quant_code<7>(acc[k][j], bs)) & 15u) << (4 * j);
+        __stcs(reinterpret_cast<unsigned int *>(out_codes + o / 2), packed);
+        if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
+    }
+}
+
+template <int B>
+static cudaError_t launch_drq_b(const uint8_t *codes, const float *scales, uint8_t *out_codes,
+                                float *out_scales, const QgzGeometry &geo,
+                                cudaStream_t stream) {
+    constexpr int T = B >= 256 ? B : 256;
+    const uint32_t total_out = geo.G * geo.N;
+    const uint32_t tiles = (total_out + T - 1) / T;
+    const uint32_t threads = 256;
+    const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
+    dequant_reduce_requant_kernel<B><<<grid, threads, 0, stream>>>(codes, scales, out_codes,
+                                                                    out_scales, geo);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *scales,
+                                          uint8_t *out_codes, float *out_scales,
+                                          const QgzGeometry &geo, int B, cudaStream_t stream) {
+    switch (B) {
+        case 32: return launch_drq_b<32>(codes, scales, out_codes, out_scales, geo, stream);
+        case 64: return launch_drq_b<64>(codes, scales, out_codes, out_scales, geo, stream);
+        case 128: return launch_drq_b<128>(codes, scales, out_codes, out_scales, geo, stream);
+        case 256: return launch_drq_b<256>(codes, scales, out_codes, out_scales, geo, stream);
+        case 512: return launch_drq_b<512>(codes, scales, out_codes, out_scales, geo, stream);
+        case 1024: return launch_drq_b<1024>(codes, scales, out_codes, out_scales, geo, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace wc

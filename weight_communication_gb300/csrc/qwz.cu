@@ -1,0 +1,121 @@
+// qwz.cu -- qwZ int8 block weight quantization and dequantization.
+//
+// "ZeROPlusPlus.md", §1.2 ZeRO++ (quantized weight communication): the
+// weights are quantized fp16 -> int8 before the forward all-gather, halving
+// its volume, with block-based quantization (an independent scale per block
+// of weights) to keep accuracy.  Here the weights are bf16.
+//
+// Quantization: one warp per block (a lane group per block for blocks shorter
+// than the warp tile); lane t holds weights 256*k + 8*t + j, i.e. 16-byte
+// bf16 loads and 8-byte code stores, both fully coalesced.  The raw bf16
+// words stay in registers between the absmax pass and the code pass.
+// Dequantization: one thread per 8 weights, 8-byte code load, 16-byte store.
+#include "wc_device.cuh"
+#include "wc_internal.h"
+
+namespace wc {
+
+template <int B>
+__global__ void __launch_bounds__(256)
+qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes,
+                      float *__restrict__ scales, uint32_t n) {
+    constexpr int T = B >= 256 ? B : 256;
+    constexpr int K = T / 256;
+    constexpr int LPB = B >= 256 ? 32 : B / 8;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    if (uint64_t(warp) * T >= n) return;
+    const uint32_t tile0 = warp * uint32_t(T);
+
+    uint4 raw[K];
+    bool active[K];
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const uint32_t x = tile0 + 256u * k + 8u * lane;
+        active[k] = x < n;
+        raw[k] = active[k] ? ld_stream_u4(w + x) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t *h = &raw[k].x;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(h[j] & 0xFFFFu)));
+            m = fmaxf(m, fabsf(bf16_bits_to_f32(h[j] >> 16)));
+        }
+    }
+    m = group_max<LPB>(m);
+    const BlockScale bs = block_scale<127>(m);
+
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (!active[k]) continue;
+        const uint32_t x = tile0 + 256u * k + 8u * lane;
+        const uint32_t *h = &raw[k].x;
+        uint32_t word[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t half = (j & 1) ? (h[j / 2] >> 16) : (h[j / 2] & 0xFFFFu);
+            const int q = quant_code<127>(bf16_bits_to_f32(half), bs);
+            word[j / 4] |= (uint32_t(q) & 0xFFu) << (8 * (j % 4));
+        }
+        __stcs(reinterpret_cast<uint2 *>(codes + x), make_uint2(word[0], word[1]));
+        if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(scales + x / B, bs.scale);
+    }
+}
+
+__global__ void __launch_bounds__(256)
+qwz_dequant_int8_kernel(const int8_t *__restrict__ codes, const float *__restrict__ scales,
+                        uint16_t *__restrict__ w_out, uint32_t n, uint32_t log2_b) {
+    const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (uint64_t(v) * 8u >= n) return;
+    const uint32_t x = v * 8u;
+    const uint2 q = ld_stream_u2(codes + x);
+    const float sc = __ldg(scales + (x >> log2_b));
+    const uint32_t qw[2] = {q.x, q.y};
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int code = int(qw[j / 4] << (24 - 8 * (j % 4))) >> 24;  // sign-extend byte
+        h[j] = f32_to_bf16_bits(dequant(code, sc));
+    }
+    __stcs(reinterpret_cast<uint4 *>(w_out + x),
+           make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                      h[6] | (h[7] << 16)));
+}
+
+template <int B>
+static cudaError_t launch_qwz_quant_b(const uint16_t *w, int8_t *codes, float *scales,
+                                      uint32_t n, cudaStream_t stream) {
+    constexpr int T = B >= 256 ? B : 256;
+    const uint32_t tiles = (n + T - 1) / T;
+    const uint32_t threads = 256;
+    const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
+    qwz_quant_int8_kernel<B><<<grid, threads, 0, stream>>>(w, codes, scales, n);
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, uint32_t n,
+                                  int B, cudaStream_t stream) {
+    switch (B) {
+        case 32: return launch_qwz_quant_b<32>(w, codes, scales, n, stream);
+        case 64: return launch_qwz_quant_b<64>(w, codes, scales, n, stream);
+        case 128: return launch_qwz_quant_b<128>(w, codes, scales, n, stream);
+        case 256: return launch_qwz_quant_b<256>(w, codes, scales, n, stream);
+        case 512: return launch_qwz_quant_b<512>(w, codes, scales, n, stream);
+        case 1024: return launch_qwz_quant_b<1024>(w, codes, scales, n, stream);
+        case 2048: return launch_qwz_quant_b<2048>(w, codes, scales, n, stream);
+        case 4096: return launch_qwz_quant_b<4096>(w, codes, scales, n, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_qwz_dequant_int8(const int8_t *codes, const float *scales, uint16_t *w_out,
+                                    uint32_t n, int B, cudaStream_t stream) {
+    uint32_t log2_b = 0;
+    while ((1u << log2_b) < uint32_t(B)) ++log2_b;
+    const uint32_t threads = 256;
+    const uint32_t grid = (n / 8 + threads - 1) / threads;
+    qwz_dequant_int8_kernel<<<grid, threads, 0, stream>>>(codes, scales, w_out, n, log2_b);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace wc

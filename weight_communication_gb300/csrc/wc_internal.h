@@ -1,0 +1,39 @@
+// wc_internal.h -- launchers shared between the kernel files and the C ABI.
+// Arguments reaching these have been validated by the ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wc {
+
+// Sizes of one qgZ problem.  All element indices fit in 32 bits: the ABI
+// rejects R*N >= 2^32.
+struct QgzGeometry {
+    uint32_t N;                // elements per rank
+    uint32_t S;                // slice (shard) length, N / R
+    uint32_t R;                // ranks
+    uint32_t G;                // groups
+    uint32_t L;                // ranks per group, R / G
+    uint32_t blocks_per_rank;  // N / B
+    uint32_t total;            // R * N
+};
+
+cudaError_t launch_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                                 const QgzGeometry &geo, int B, float s, float beta,
+                                 cudaStream_t stream);
+cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
+                                  const QgzGeometry &geo, int B, float out_scale, void *out,
+                                  bool out_bf16, cudaStream_t stream);
+cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *scales,
+                                          uint8_t *out_codes, float *out_scales,
+                                          const QgzGeometry &geo, int B, cudaStream_t stream);
+cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, uint32_t n,
+                                  int B, cudaStream_t stream);
+cudaError_t launch_qwz_dequant_int8(const int8_t *codes, const float *scales, uint16_t *w_out,
+                                    uint32_t n, int B, cudaStream_t stream);
+cudaError_t launch_sr_accumulate(uint16_t *dst, uint16_t *src, uint32_t n, uint32_t seed,
+                                 uint32_t step, cudaStream_t stream);
+uint32_t sr_key(uint32_t seed, uint32_t step);
+
+}  // namespace wc

@@ -1,0 +1,84 @@
+"""One qgZ reduce step over R simulated ranks, composed from the C-ABI calls.
+
+ZeROPlusPlus.md §1.2 (quantized gradient communication): each rank
+block-quantizes its gradient to int4, an all-to-all replaces the
+reduce-scatter, and the receivers reduce in full precision -- flat, or
+intra-group first and inter-group second.  "Merge LoCo with Zero++" (DeepSpeed
+PR #6730), Overview: the gradient is compensated with the rank's
+error-feedback buffer before quantization, at the cost of that buffer's
+memory and no extra time.
+
+`QgzReducer` owns the device buffers of one problem (error feedback, send
+buffers, first-hop buffers, reduced shards) and runs a step as 2 launches
+(flat) or 3 launches (hierarchical) on one stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding
+
+
+class QgzReducer:
+    """Device state and launches of one (R, N, G, B) quantized reduce.
+
+    error feedback : fp32 [R, N], persistent across steps (zeroed at start)
+    codes, scales  : int4 send buffers [R, N/2] bytes and [R, N/B] fp32
+    hop1 codes/sc. : first-hop outputs [G*N/2], [G*N/B] (G > 1 only)
+    out            : reduced shards [N] (= [R][S]), fp32 or bf16
+    """
+
+    def __init__(self, N: int, R: int, G: int = 1, B: int = 256, err_scale: float = 1.0,
+                 err_beta: float = 0.0, use_ef: bool = True, out_dtype=torch.float32,
+                 out_scale: float = 1.0, device="cuda"):
+        self.N, self.R, self.G, self.B = N, R, G, B
+        self.err_scale, self.err_beta = err_scale, err_beta
+        self.out_scale = out_scale
+        self.device = torch.device(device)
+        dev = self.device
+        self.ef = torch.zeros(R * N, dtype=torch.float32, device=dev) if use_ef else None
+        self.codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+        if G > 1:
+            self.codes1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+            self.scales1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+        else:
+            self.codes1 = self.scales1 = None
+        self.out = torch.empty(N, dtype=out_dtype, device=dev)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 3 if self.G > 1 else 2
+
+    def quantize(self, g: torch.Tensor, stream=None) -> None:
+        binding.ef_quant_int4(g.reshape(-1), self.ef, self.codes, self.scales, self.N, self.R,
+                              self.G, self.B, self.err_scale, self.err_beta, stream)
+
+    def reduce(self, stream=None) -> torch.Tensor:
+        if self.G > 1:
+            binding.dequant_reduce_requant(self.codes, self.scales, self.codes1, self.scales1,
+                                           self.N, self.R, self.G, self.B, stream)
+            binding.dequant_reduce(self.codes1, self.scales1, self.out, self.N, self.R, self.G,
+                                   self.B, self.out_scale, stream)
+        else:
+            binding.dequant_reduce(self.codes, self.scales, self.out, self.N, self.R, 1, self.B,
+                                   self.out_scale, stream)
+        return self.out
+
+    def step(self, g: torch.Tensor, stream=None) -> torch.Tensor:
+        """Quantize every rank's gradient g ([R, N] bf16 on the device) and
+        reduce; returns the [N] reduced shards (destination-major)."""
+        self.quantize(g, stream)
+        return self.reduce(stream)
+
+    def step_host(self, g_host: torch.Tensor, g_dev: torch.Tensor, out_host: torch.Tensor,
+                  stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+        """End-to-end step from host memory: copy g_host (pinned, [R, N] bf16)
+        into g_dev, run the step, copy the shards into out_host (pinned), all
+        on one stream; the caller synchronizes."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            g_dev.copy_(g_host, non_blocking=True)
+            self.step(g_dev, s)
+            out_host.copy_(self.out, non_blocking=True)
+        return out_host
