@@ -80,6 +80,12 @@ def sum_over_ranks(value: float, dist, device) -> float:
     return float(t.item())
 
 
+def job_throughput(units_per_rank_step: float, ws: int, max_ms_per_step: float) -> float:
+    """Whole-job rate: every replica processes the same units per step and
+    the job advances at the pace of the slowest rank."""
+    return units_per_rank_step * ws / (max_ms_per_step / 1e3)
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -142,12 +148,17 @@ class ClockSampler:
         self.file.flush()
         rows = Path(self.file.name).read_text().splitlines()
         os.unlink(self.file.name)
-        sm, smax, reasons, n_all = [], [], set(), 0
+        return self.parse(rows, t0, t1)
+
+    @classmethod
+    def parse(cls, rows, t0: float, t1: float):
+        """Median SM clock, max clock and active throttle reasons of the
+        samples taken between host times t0 and t1."""
+        sm, smax, reasons = [], [], set()
         for row in rows:
             f = [x.strip() for x in row.split(",")]
             if len(f) < 9:
                 continue
-            n_all += 1
             try:
                 ts = _dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
             except ValueError:
@@ -159,7 +170,7 @@ class ClockSampler:
                 smax.append(float(f[2]))
             except ValueError:
                 continue
-            for name, v in zip(self.REASONS, f[5:9]):
+            for name, v in zip(cls.REASONS, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -300,7 +311,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws):
     ms_local = timer.step_sum_ms() if flush is not None else start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms_local, dist, dev)
     units = w.R * w.N
-    value = units * ws / (ms / 1e3)
+    value = job_throughput(units, ws, ms)
 
     # roofline of the dominant kernel (the error-feedback quantization)
     peak, peak_kind = measured_peaks()
