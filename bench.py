@@ -195,6 +195,8 @@ KERNEL_SOURCES = {
                          "weight_communication_gb300/csrc/wc_device.cuh"],
     "sr_accumulate": ["weight_communication_gb300/csrc/sr_accumulate.cu",
                       "weight_communication_gb300/csrc/wc_device.cuh"],
+    "qgz_step_fused": ["weight_communication_gb300/csrc/qgz_fused.cu",
+                       "weight_communication_gb300/csrc/wc_device.cuh"],
 }
 
 
@@ -355,6 +357,58 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws):
     if not args.no_e2e:
         line["e2e"] = run_qgz_e2e(w, red, batches[0], args, dev, dist, ws, stream)
     return line, batches[0]
+
+
+def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
+    """The flat step as one fused launch (EF-quant of every rank + reduce),
+    writing the error buffers, the send buffers and the shards."""
+    from weight_communication_gb300 import binding
+    assert w.G == 1
+    out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+    ef = torch.zeros(w.R * w.N, dtype=torch.float32, device=dev)
+    codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+    out = torch.empty(w.N, dtype=out_dtype, device=dev)
+    nbatch = max(1, min(args.batches, (8 << 30) // (w.R * w.N * 2)))
+    batches = [wl.qgz_gradients(w, t, device=dev) for t in range(nbatch)]
+    stream = torch.cuda.Stream(dev)
+    names = ["qgz_step_fused"]
+    with torch.cuda.stream(stream):
+        def step(i):
+            binding.qgz_step_fused(batches[i % nbatch].view(-1), ef, codes, scales, out, w.N,
+                                   w.R, w.B, w.err_scale, w.err_beta, 1.0, stream)
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        timer = Timer(names, args.steps)
+        barrier(dist)
+        for i in range(args.steps):
+            timer.mark(i, 0)
+            step(args.warmup + i)
+            timer.mark(i, 1)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+    ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
+    peak, kind = measured_peaks()
+    b = w.R * w.N * (2 + 4 + 4 + 0.5) + w.R * w.N // w.B * 4 + w.N * (2 if w.out_bf16 else 4)
+    achieved = b / (ms / 1e3) / 1e9
+    return {"metric": METRIC + " [fused single kernel]", "value": job_throughput(w.R * w.N, ws, ms),
+            "unit": "elements/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded normal gradients with sparse outliers)",
+            "config": {"workload": w.name + " fused", "R": w.R, "N": w.N, "G": 1, "B": w.B,
+                       "err_scale": w.err_scale, "err_beta": w.err_beta,
+                       "l2": f"inputs exceed L2 ({w.R * w.N * 10 / 1e9:.1f} GB per step)"},
+            "roofline": {"bound": "hbm", "kernel": "qgz_step_fused", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
+                         "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic("qgz_step_fused", "qgz_single_hop", w.R * w.N)
+                         if "qgz_step_fused" in KERNEL_SOURCES else None,
+                         "algorithmic_bytes": int(b)},
+            "kernels": {"qgz_step_fused": {"ms": round(ms, 5), "algorithmic_bytes": int(b),
+                                           "GB/s": round(achieved, 1),
+                                           "frac": round(achieved / peak, 4)}},
+            "gpu_launches": args.steps}, None
 
 
 def run_qgz_e2e(w, red, g_example, args, dev, dist, ws, stream):
@@ -566,7 +620,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
-                    choices=["qgz_single_hop", "qgz_tiny", "qgz_hierarchical", "qwz", "sr", "all"])
+                    choices=["qgz_single_hop", "qgz_fused", "qgz_tiny", "qgz_hierarchical",
+                             "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
@@ -593,10 +648,13 @@ def main(argv=None):
     from weight_communication_gb300 import binding
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
-    names = (["qgz_single_hop", "qgz_tiny", "qgz_hierarchical", "qwz", "sr"]
+    names = (["qgz_single_hop", "qgz_fused", "qgz_tiny", "qgz_hierarchical", "qwz", "sr"]
              if args.workload == "all" else [args.workload])
     for name in names:
-        if name in wl.QGZ_WORKLOADS:
+        if name == "qgz_fused":
+            w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
+            line, _ = run_qgz_fused(w, args, dev, dist, ws)
+        elif name in wl.QGZ_WORKLOADS:
             w = wl.QGZ_WORKLOADS[name]
             if args.scale > 1:
                 w = qgz_sample(w, args.scale)

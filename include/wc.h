@@ -147,6 +147,25 @@ WC_API int wc_dequant_reduce_requant(const uint8_t *codes, const float *scales,
                                      void *stream);
 
 /*
+ * wc_qgz_step_fused -- the whole flat step (G = 1) in one kernel: for every
+ * destination block it runs wc_ef_quant_int4's arithmetic on the R ranks in
+ * rank order and adds their dequantized values as wc_dequant_reduce does, so
+ * out, ef, codes and scales are bit-identical to calling the two in
+ * sequence, while the codes never have to be read back from memory.
+ * ("ZeROPlusPlus.md" §1.2: qgZ with CUDA kernel fusion; with every rank in
+ * one GPU's memory the fusion can span the all-to-all.)
+ * g, ef    : as wc_ef_quant_int4 (ef may be NULL).
+ * codes, scales : the send buffers as wc_ef_quant_int4 writes them with G = 1,
+ *           or both NULL to skip writing them.
+ * out      : [R][S] fp32 or bf16 (out_dtype), destination order.
+ * Requires the sizes of wc_ef_quant_int4 with G = 1 and B >= 128.
+ */
+WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes,
+                             float *scales, int64_t N, int R, int B,
+                             float err_scale, float err_beta, float out_scale,
+                             void *out, int out_dtype, void *stream);
+
+/*
  * wc_qwz_quant_int8 -- qwZ block weight quantization (step a10).
  * Per block of B weights (bf16 widened exactly to fp32), m = max |w|:
  *   m < 127 * 2^-126: scale = 0, q = 0

@@ -70,6 +70,11 @@ _SIGS = {
     "orc_dequant_reduce": (None, [_P, _P, _I64, _I, _I, _I, _F, _P, _I]),
     "orc_dequant_reduce_requant_unit": (None, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P]),
     "orc_dequant_reduce_requant": (None, [_P, _P, _I64, _I, _I, _I, _P, _P]),
+    "orc_dequant_reduce_requant_unit_ef": (None, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _P, _F, _F]),
+    "orc_dequant_reduce_requant_ef": (None, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F]),
+    "orc_ef_quant_int4_rank_bf16ef": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_bf16ef": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_qwz_quant_replica_int8": (None, [_P, _P, _P, _P, _I64, _I]),
     "orc_qwz_quant_int8": (None, [_P, _P, _P, _I64, _I]),
     "orc_qwz_dequant_int8": (None, [_P, _P, _P, _I64, _I]),
     "orc_fmix32": (_U32, [_U32]),
@@ -225,6 +230,48 @@ class Oracle:
                                                   B, g, l, _ptr(oc), _ptr(os_))
         return oc, os_
 
+    def dequant_reduce_requant_ef(self, codes, scales, N, R, G, B, e1, s, beta):
+        """Hop 1 with error feedback on the requantization; e1 float32
+        [R*G*S] (unit order) updated in place, or None."""
+        S, _, _ = _check_qgz(N, R, G, B)
+        if e1 is not None:
+            assert e1.dtype == np.float32 and e1.size == R * G * S
+        oc = np.zeros(R * G * S // 2, dtype=np.uint8)
+        os_ = np.zeros(R * G * S // B, dtype=np.float32)
+        self._lib.orc_dequant_reduce_requant_ef(_ptr(codes), _ptr(scales), N, R, G, B,
+                                                _ptr(oc), _ptr(os_), _ptr(e1), s, beta)
+        return oc, os_
+
+    def dequant_reduce_requant_unit_ef(self, codes, scales, N, R, G, B, g, l, e1u, s, beta):
+        """Hop 1 with error feedback, unit (g, l); e1u float32 [G*S] in place."""
+        S, _, _ = _check_qgz(N, R, G, B)
+        oc = np.zeros(G * S // 2, dtype=np.uint8)
+        os_ = np.zeros(G * S // B, dtype=np.float32)
+        self._lib.orc_dequant_reduce_requant_unit_ef(_ptr(codes), _ptr(scales), N, R, G, B,
+                                                     g, l, _ptr(oc), _ptr(os_), _ptr(e1u),
+                                                     s, beta)
+        return oc, os_
+
+    def ef_quant_int4_bf16ef(self, g: np.ndarray, e16: np.ndarray, N: int, R: int, G: int,
+                             B: int, s: float, beta: float):
+        """All ranks with a bf16 error buffer (uint16 [R*N], in place)."""
+        _check_qgz(N, R, G, B)
+        assert g.dtype == np.uint16 and g.size == R * N
+        assert e16.dtype == np.uint16 and e16.size == R * N
+        codes = np.zeros(R * N // 2, dtype=np.uint8)
+        scales = np.zeros(R * N // B, dtype=np.float32)
+        self._lib.orc_ef_quant_int4_bf16ef(_ptr(g), _ptr(e16), _ptr(codes), _ptr(scales),
+                                           N, R, G, B, s, beta)
+        return codes, scales
+
+    def ef_quant_int4_rank_bf16ef(self, g_r, e16_r, N, R, G, B, s, beta):
+        _check_qgz(N, R, G, B)
+        codes = np.zeros(N // 2, dtype=np.uint8)
+        scales = np.zeros(N // B, dtype=np.float32)
+        self._lib.orc_ef_quant_int4_rank_bf16ef(_ptr(g_r), _ptr(e16_r), _ptr(codes),
+                                                _ptr(scales), N, R, G, B, s, beta)
+        return codes, scales
+
     # -- qwZ --------------------------------------------------------------
     def qwz_quant_int8(self, w: np.ndarray, B: int):
         n = w.size
@@ -241,6 +288,17 @@ class Oracle:
         out = np.zeros(n, dtype=np.uint16)
         self._lib.orc_qwz_dequant_int8(_ptr(codes), _ptr(scales), _ptr(out), n, B)
         return out
+
+    def qwz_quant_replica_int8(self, w: np.ndarray, B: int):
+        """(codes, scales, bf16 replica) of the weights."""
+        n = w.size
+        if B < 1 or B > MAX_BLOCK or n % B:
+            raise ValueError(f"B must divide n and be <= {MAX_BLOCK}")
+        codes = np.zeros(n, dtype=np.int8)
+        scales = np.zeros(n // B, dtype=np.float32)
+        rep = np.zeros(n, dtype=np.uint16)
+        self._lib.orc_qwz_quant_replica_int8(_ptr(w), _ptr(codes), _ptr(scales), _ptr(rep), n, B)
+        return codes, scales, rep
 
     # -- SR accumulate ------------------------------------------------------
     def sr_accumulate_bf16(self, dst: np.ndarray, src: np.ndarray, seed: int, step: int):

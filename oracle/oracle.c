@@ -242,6 +242,63 @@ ORC_EXPORT void orc_ef_quant_int4(const uint16_t *g, float *e,
                                N, R, G, B, s, beta);
 }
 
+/*
+ * The same step with a bf16 error buffer.  LoCo's cost is the extra memory of
+ * the error buffer ("Merge LoCo with Zero++", Overview); storing it in bf16
+ * halves that memory and its traffic.  Reading: the stored error is widened
+ * exactly, every operation is the binary32 chain of orc_ef_quant_int4_rank,
+ * and only the new error is rounded to the nearest bf16 (ties to even) when
+ * it is stored.  e16: N bf16 bit patterns, in place (not NULL).
+ */
+ORC_EXPORT void orc_ef_quant_int4_rank_bf16ef(const uint16_t *g, uint16_t *e16,
+                                              uint8_t *codes, float *scales,
+                                              int64_t N, int R, int G, int B,
+                                              float s, float beta)
+{
+    int64_t S = N / R;
+    float omb = 1.0f - beta;
+    float c[8192];
+    int8_t q[8192];
+    for (int64_t slice = 0; slice < R; ++slice) {
+        int64_t p = orc_send_position(slice, R, G);
+        for (int64_t b0 = 0; b0 < S; b0 += B) {
+            int64_t in0 = slice * S + b0;
+            int64_t out0 = p * S + b0;
+            for (int i = 0; i < B; ++i) {
+                float gh = orc_bf16_to_f32(g[in0 + i]);
+                float eh = orc_bf16_to_f32(e16[in0 + i]);
+                float seh = s * eh;
+                c[i] = gh + seh;
+            }
+            float scale;
+            orc_quant_block(c, B, 7, q, &scale);
+            scales[out0 / B] = scale;
+            for (int i = 0; i < B; ++i)
+                put_nibble(codes, out0 + i, q[i]);
+            for (int i = 0; i < B; ++i) {
+                float eh = orc_bf16_to_f32(e16[in0 + i]);
+                float dh = orc_dequant(q[i], scale);
+                float rh = c[i] - dh;
+                float kh = beta * eh;
+                float ah = omb * rh;
+                e16[in0 + i] = orc_f32_to_bf16_rne(kh + ah);
+            }
+        }
+    }
+}
+
+ORC_EXPORT void orc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *e16,
+                                         uint8_t *codes, float *scales,
+                                         int64_t N, int R, int G, int B,
+                                         float s, float beta)
+{
+    for (int r = 0; r < R; ++r)
+        orc_ef_quant_int4_rank_bf16ef(g + (int64_t)r * N, e16 + (int64_t)r * N,
+                                      codes + (int64_t)r * (N / 2),
+                                      scales + (int64_t)r * (N / B),
+                                      N, R, G, B, s, beta);
+}
+
 /* ------------------------------------------------------------------------ */
 /* a6-a7 / a9: dequantize and reduce in full precision                        */
 /* ------------------------------------------------------------------------ */
@@ -321,6 +378,14 @@ ORC_EXPORT void orc_dequant_reduce(const uint8_t *codes, const float *scales,
  * error feedback on this hop.  Output: G*S codes (G*S/2 bytes) and G*S/B
  * scales, sub-slice g' first-to-last; sub-slice g' is bound for rank g'*L + l.
  */
+ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
+                                                   const float *scales,
+                                                   int64_t N, int R, int G, int B,
+                                                   int g, int l,
+                                                   uint8_t *out_codes,
+                                                   float *out_scales,
+                                                   float *e1, float s, float beta);
+
 ORC_EXPORT void orc_dequant_reduce_requant_unit(const uint8_t *codes,
                                                 const float *scales,
                                                 int64_t N, int R, int G, int B,
@@ -328,12 +393,35 @@ ORC_EXPORT void orc_dequant_reduce_requant_unit(const uint8_t *codes,
                                                 uint8_t *out_codes,
                                                 float *out_scales)
 {
+    orc_dequant_reduce_requant_unit_ef(codes, scales, N, R, G, B, g, l,
+                                       out_codes, out_scales, 0, 0.0f, 0.0f);
+}
+
+/*
+ * The same first hop with error feedback on the requantization ("Merge LoCo
+ * with Zero++", review thread: the error buffers hang off each parameter as
+ * `inter_ef_buf`, the buffer of the inter-node message).  Reading: the unit
+ * keeps one fp32 error per requantized value, e1 [G*S] in output order, and
+ * applies the update of orc_ef_quant_int4_rank to the partial sums:
+ *   c = p + s * e1;  q, scale = Q4(c);  e1 <- beta * e1 + (1 - beta) * (c - d).
+ * e1 == NULL is the plain first hop.
+ */
+ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
+                                                   const float *scales,
+                                                   int64_t N, int R, int G, int B,
+                                                   int g, int l,
+                                                   uint8_t *out_codes,
+                                                   float *out_scales,
+                                                   float *e1, float s, float beta)
+{
     int64_t S = N / R;
     int L = R / G;
+    float one_minus_beta = 1.0f - beta;
     float part[8192];
     int8_t q[8192];
     for (int gq = 0; gq < G; ++gq) {
         for (int64_t b0 = 0; b0 < S; b0 += B) {
+            int64_t out0 = (int64_t)gq * S + b0;
             for (int i = 0; i < B; ++i) {
                 float acc = 0.0f;
                 for (int lq = 0; lq < L; ++lq) {
@@ -341,34 +429,60 @@ ORC_EXPORT void orc_dequant_reduce_requant_unit(const uint8_t *codes,
                     int64_t pos = r * N + ((int64_t)l * G + gq) * S + b0 + i;
                     acc = acc + dq_at(codes, scales, pos, B);
                 }
+                if (e1) {
+                    float se1 = s * e1[out0 + i];
+                    acc = acc + se1;
+                }
                 part[i] = acc;
             }
             float scale;
             orc_quant_block(part, B, 7, q, &scale);
-            int64_t out0 = (int64_t)gq * S + b0;
             out_scales[out0 / B] = scale;
             for (int i = 0; i < B; ++i)
                 put_nibble(out_codes, out0 + i, q[i]);
+            if (e1) {
+                for (int i = 0; i < B; ++i) {
+                    float d1 = orc_dequant(q[i], scale);
+                    float resid1 = part[i] - d1;
+                    float kept1 = beta * e1[out0 + i];
+                    float added1 = one_minus_beta * resid1;
+                    e1[out0 + i] = kept1 + added1;
+                }
+            }
         }
     }
 }
 
-/* Every unit: out_codes is [R][G*S/2], out_scales [R][G*S/B], unit g*L + l. */
-ORC_EXPORT void orc_dequant_reduce_requant(const uint8_t *codes,
-                                           const float *scales,
-                                           int64_t N, int R, int G, int B,
-                                           uint8_t *out_codes,
-                                           float *out_scales)
+/* Every unit: out_codes is [R][G*S/2], out_scales [R][G*S/B], unit g*L + l;
+ * e1 (or NULL) is [R][G*S] in the same unit order. */
+ORC_EXPORT void orc_dequant_reduce_requant_ef(const uint8_t *codes,
+                                              const float *scales,
+                                              int64_t N, int R, int G, int B,
+                                              uint8_t *out_codes,
+                                              float *out_scales,
+                                              float *e1, float s, float beta)
 {
     int64_t S = N / R;
     int L = R / G;
     for (int g = 0; g < G; ++g)
         for (int l = 0; l < L; ++l) {
             int64_t unit = (int64_t)g * L + l;
-            orc_dequant_reduce_requant_unit(codes, scales, N, R, G, B, g, l,
-                                            out_codes + unit * (G * S / 2),
-                                            out_scales + unit * (G * S / B));
+            orc_dequant_reduce_requant_unit_ef(codes, scales, N, R, G, B, g, l,
+                                               out_codes + unit * (G * S / 2),
+                                               out_scales + unit * (G * S / B),
+                                               e1 ? e1 + unit * (G * S) : 0,
+                                               s, beta);
         }
+}
+
+ORC_EXPORT void orc_dequant_reduce_requant(const uint8_t *codes,
+                                           const float *scales,
+                                           int64_t N, int R, int G, int B,
+                                           uint8_t *out_codes,
+                                           float *out_scales)
+{
+    orc_dequant_reduce_requant_ef(codes, scales, N, R, G, B, out_codes,
+                                  out_scales, 0, 0.0f, 0.0f);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -392,6 +506,18 @@ ORC_EXPORT void orc_qwz_dequant_int8(const int8_t *codes, const float *scales,
 {
     for (int64_t i = 0; i < n; ++i)
         w_out[i] = orc_f32_to_bf16_rne(orc_dequant(codes[i], scales[i / B]));
+}
+
+/* qwZ quantization that also writes the bf16 weights the codes stand for:
+ * the copy a node keeps after the forward all-gather (the hierarchical
+ * partition of "ZeROPlusPlus.md" §1.2 keeps a full model copy in each node).
+ * Exactly orc_qwz_quant_int8 followed by orc_qwz_dequant_int8. */
+ORC_EXPORT void orc_qwz_quant_replica_int8(const uint16_t *w, int8_t *codes,
+                                           float *scales, uint16_t *replica,
+                                           int64_t n, int B)
+{
+    orc_qwz_quant_int8(w, codes, scales, n, B);
+    orc_qwz_dequant_int8(codes, scales, replica, n, B);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -120,3 +120,21 @@ def test_binding_rejects_cpu_tensors(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         binding.load(tmp_path / "libwc.so")
+
+
+def test_fused_step_argument_errors(lib):
+    f = lib.wc_qgz_step_fused
+    ok = (FAKE, FAKE, FAKE, FAKE, 8192, 8, 256, 1.0, 0.5, 1.0, FAKE, 0, None)
+    def call(**kw):
+        a = list(ok)
+        names = ["g", "ef", "codes", "scales", "N", "R", "B", "s", "beta", "os", "out", "dt", "st"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+    assert call(B=64) == binding.WC_EINVAL                 # below 128
+    assert call(codes=None) == binding.WC_EINVAL           # codes without scales
+    assert call(dt=3) == binding.WC_EINVAL
+    assert call(out=MIS) == binding.WC_EALIGN
+    assert call(ef=MIS) == binding.WC_EALIGN
+    assert call(g=None) == binding.WC_EINVAL
+    assert call(N=0, g=None, out=None) == binding.WC_OK

@@ -15,7 +15,7 @@ import pytest
 import oracle
 
 ROOT = Path(__file__).resolve().parent.parent
-PIN_FILES = ["tests/test_oracle_qgz.py", "tests/test_oracle_sr.py",
+PIN_FILES = ["tests/test_oracle_qgz.py", "tests/test_oracle_next.py", "tests/test_oracle_sr.py",
              "tests/test_oracle_qwz.py", "tests/test_oracle_bf16.py",
              "tests/test_oracle_quant.py"]
 
@@ -56,6 +56,15 @@ MUTANTS = {
     "sr_src_not_zeroed": ("        src[i] = 0;\n", "\n"),
     "sr_sum_dropped_src": ("float sum = orc_bf16_to_f32(dst[i]) + orc_bf16_to_f32(src[i]);",
                            "float sum = orc_bf16_to_f32(dst[i]);"),
+    "hop1_ef_residual_sign": ("float resid1 = part[i] - d1;", "float resid1 = d1 - part[i];"),
+    "hop1_ef_scale_dropped": ("float se1 = s * e1[out0 + i];", "float se1 = e1[out0 + i];"),
+    "hop1_ef_beta_swapped": ("float kept1 = beta * e1[out0 + i];",
+                             "float kept1 = one_minus_beta * e1[out0 + i];"),
+    "bf16ef_truncates": ("e16[in0 + i] = orc_f32_to_bf16_rne(kh + ah);",
+                         "e16[in0 + i] = (uint16_t)(f32_bits(kh + ah) >> 16);"),
+    "bf16ef_beta_swapped": ("float kh = beta * eh;", "float kh = omb * eh;"),
+    "bf16ef_compensation_sign": ("c[i] = gh + seh;", "c[i] = gh - seh;"),
+    "replica_skips_dequant": ("    orc_qwz_dequant_int8(codes, scales, replica, n, B);\n", "\n"),
     "fmix_constant": ("h *= 0x85EBCA6Bu;", "h *= 0x85EBCA6Cu;"),
     "fmix_shift": ("h ^= h >> 13;", "h ^= h >> 12;"),
 }

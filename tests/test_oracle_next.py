@@ -1,0 +1,194 @@
+"""Pins for the oracle's extensions beyond the basic path:
+
+  * error feedback on the first hop's requantization ("Merge LoCo with
+    Zero++", review thread: `inter_ef_buf`, the error buffer of the
+    inter-node message) -- a hand-worked exact case, zero error = plain hop,
+    the telescoping identity over steps with plain error feedback, and the
+    LoCo recurrence bound;
+  * a bf16 error buffer (the memory LoCo costs, "Merge LoCo with Zero++",
+    Overview) -- one step equals the fp32-buffer step with only the stored
+    error rounded to bf16 by torch's conversion; over several steps the
+    telescoping identity holds up to the bf16 storage rounding;
+  * qwZ quantization with the bf16 replica written alongside
+    (ZeROPlusPlus.md §1.2) -- equal to quantize then dequantize.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact import unpack_int4
+from weight_communication_gb300 import workloads as wl
+
+
+def _deq(codes, scales, B):
+    return unpack_int4(codes).astype(np.float64) * np.repeat(scales.astype(np.float64), B)
+
+
+def _bf16(vals):
+    return wl.as_u16(torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16)).copy()
+
+
+# --------------------------------------------------------------------------
+# first-hop error feedback
+# --------------------------------------------------------------------------
+
+def test_first_hop_error_feedback_worked_example(orc):
+    # R = 2 ranks, one group (L = 2), B = S = 2, N = 4.  Unit (0, 0) adds
+    # chunk 0 of both ranks: rank 0 codes (7, 1), rank 1 codes (0, 2), scale 1
+    # -> partial sums p = (7, 3).  With e1 = (0, 0.25), s = 2, beta = 0.25:
+    # c = (7, 3.5), absmax 7 -> scale 1, q = (7, rint(3.5) = 4), d = (7, 4),
+    # c - d = (0, -0.5), e1' = (0, 0.25*0.25 + 0.75*(-0.5)) = (0, -0.3125).
+    codes = np.array([0x17, 0x00, 0x20, 0x00], np.uint8)
+    scales = np.ones(4, np.float32)
+    e1 = np.array([0.0, 0.25], np.float32)
+    oc, os_ = orc.dequant_reduce_requant_unit_ef(codes, scales, 4, 2, 1, 2, 0, 0, e1, 2.0, 0.25)
+    assert unpack_int4(oc).tolist() == [7, 4]
+    assert os_.tolist() == [1.0]
+    assert e1.tolist() == [0.0, -0.3125]
+    # without the error buffer: p = (7, 3) quantizes to (7, 3)
+    oc0, _ = orc.dequant_reduce_requant_unit(codes, scales, 4, 2, 1, 2, 0, 0)
+    assert unpack_int4(oc0).tolist() == [7, 3]
+
+
+def _hop0(orc, w, t):
+    g = wl.as_u16(wl.qgz_gradients(w, t)).ravel().copy()
+    return orc.ef_quant_int4(g, None, w.N, w.R, w.G, w.B, 1.0, 0.0)
+
+
+def _partial_sums(codes, scales, w, magnitude=False):
+    """fp64 sums (or sums of magnitudes), over the L ranks of each group, of
+    the chunks every unit receives, in the unit-major [R][G][S] layout of the
+    first hop's output."""
+    R, N, G, L, S, B = w.R, w.N, w.G, w.L, w.S, w.B
+    d = _deq(codes, scales, B).reshape(R, N)
+    if magnitude:
+        d = np.abs(d)
+    p = np.zeros((R, G, S))
+    for g in range(G):
+        for l in range(L):
+            for gq in range(G):
+                ch = (l * G + gq) * S
+                p[g * L + l, gq] = d[g * L:(g + 1) * L, ch:ch + S].sum(0)
+    return p.ravel()
+
+
+def test_first_hop_error_feedback_zero_buffer_is_plain(orc):
+    w = wl.QgzWorkload(9, "t", 8, 8 * 256 * 3, 2, 256, 1.0, 0.5, 1, 1e-3, 1e-3, 100.0, True)
+    codes, scales = _hop0(orc, w, 0)
+    plain_c, plain_s = orc.dequant_reduce_requant(codes, scales, w.N, w.R, w.G, w.B)
+    e1 = np.zeros(w.G * w.N, np.float32)
+    c1, s1 = orc.dequant_reduce_requant_ef(codes, scales, w.N, w.R, w.G, w.B, e1, 1.0, 0.5)
+    assert np.array_equal(c1, plain_c) and np.array_equal(s1, plain_s)
+    c2, s2 = orc.dequant_reduce_requant_ef(codes, scales, w.N, w.R, w.G, w.B, None, 1.0, 0.5)
+    assert np.array_equal(c2, plain_c) and np.array_equal(s2, plain_s)
+    # the unit form matches the whole-buffer form
+    e_a = np.zeros(w.G * w.N, np.float32)
+    ca, sa = orc.dequant_reduce_requant_ef(codes, scales, w.N, w.R, w.G, w.B, e_a, 1.0, 0.5)
+    unit = w.G * w.S
+    for u in range(w.R):
+        g, l = divmod(u, w.L)
+        eu = np.zeros(unit, np.float32)
+        cu, su = orc.dequant_reduce_requant_unit_ef(codes, scales, w.N, w.R, w.G, w.B, g, l,
+                                                    eu, 1.0, 0.5)
+        assert np.array_equal(cu, ca[u * unit // 2:(u + 1) * unit // 2])
+        assert np.array_equal(eu, e_a[u * unit:(u + 1) * unit])
+
+
+def test_first_hop_telescoping(orc):
+    """Plain error feedback on the requantization (s = 1, beta = 0): the
+    requantized values sent over T steps add up to the partial sums received
+    plus e1_0 - e1_T."""
+    w = wl.QgzWorkload(9, "t", 8, 8 * 512 * 2, 2, 512, 1.0, 0.0, 1, 1e-3, 1e-3, 100.0, True)
+    e1 = np.zeros(w.G * w.N, np.float32)
+    sum_d = np.zeros(w.G * w.N)
+    sum_p = np.zeros(w.G * w.N)
+    mag = np.zeros(w.G * w.N)
+    for t in range(4):
+        codes, scales = _hop0(orc, w, t)
+        p = _partial_sums(codes, scales, w)
+        c1, s1 = orc.dequant_reduce_requant_ef(codes, scales, w.N, w.R, w.G, w.B, e1, 1.0, 0.0)
+        sum_d += _deq(c1, s1, w.B)
+        sum_p += p
+        mag += np.abs(p) + np.abs(e1)
+    assert np.all(np.abs(sum_d - (sum_p - e1)) <= 1e-5 * mag + 1e-30)
+    assert np.abs(e1).max() > 0
+
+
+@pytest.mark.parametrize("beta", [0.25, 0.5])
+def test_first_hop_loco_bound(orc, beta):
+    w = wl.QgzWorkload(9, "t", 8, 8 * 256 * 2, 2, 256, 1.0, beta, 1, 1e-3, 1e-3, 100.0, True)
+    e1 = np.zeros(w.G * w.N, np.float32)
+    for t in range(3):
+        codes, scales = _hop0(orc, w, t)
+        prev = e1.astype(np.float64).copy()
+        p = _partial_sums(codes, scales, w)
+        pm = _partial_sums(codes, scales, w, magnitude=True)
+        c1, s1 = orc.dequant_reduce_requant_ef(codes, scales, w.N, w.R, w.G, w.B, e1, 1.0, beta)
+        sc = np.repeat(s1.astype(np.float64), w.B)
+        bound = beta * np.abs(prev) + (1 - beta) * sc * (0.5 + 2.0**-18)
+        assert np.all(np.abs(e1) <= bound * (1 + 2.0**-20) + 1e-38)
+        # two-sided: which term beta multiplies; the fp32 partial sum rounds
+        # against the magnitude of its L terms
+        pred = beta * prev + (1 - beta) * (p + prev - _deq(c1, s1, w.B))
+        assert np.all(np.abs(e1 - pred) <= 8 * 2.0**-24 * (w.L * pm + np.abs(prev)) + 1e-38)
+
+
+# --------------------------------------------------------------------------
+# bf16 error buffer
+# --------------------------------------------------------------------------
+
+def test_bf16_error_buffer_one_step_equals_rounded_fp32(orc):
+    w = wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 4)
+    g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
+    rng = np.random.default_rng(4)
+    e_start = torch.from_numpy((rng.standard_normal(w.R * w.N) * 1e-4).astype(np.float32)) \
+        .to(torch.bfloat16)
+    e16 = wl.as_u16(e_start).copy()
+    e32 = e_start.float().numpy().copy()
+    for s, beta in ((1.0, 0.5), (1.0, 0.0), (0.5, 0.25)):
+        a16, a32 = e16.copy(), e32.copy()
+        c16, s16 = orc.ef_quant_int4_bf16ef(g, a16, w.N, w.R, w.G, w.B, s, beta)
+        c32, s32 = orc.ef_quant_int4(g, a32, w.N, w.R, w.G, w.B, s, beta)
+        assert np.array_equal(c16, c32) and np.array_equal(s16, s32)
+        want = wl.as_u16(torch.from_numpy(a32).to(torch.bfloat16))
+        assert np.array_equal(a16, want)
+
+
+def test_bf16_error_buffer_worked_example(orc):
+    # the fp32 worked example's first three errors are bf16-representable
+    g = _bf16([7.0, 1.0, -3.0, 0.5])
+    e16 = _bf16([0.0, 0.375, -0.5, 0.25])
+    codes, scales = orc.ef_quant_int4_bf16ef(g, e16, 4, 1, 1, 2, 2.0, 0.25)
+    assert unpack_int4(codes).tolist() == [7, 2, -7, 2]
+    back = (e16.astype(np.uint32) << 16).view(np.float32)
+    assert back[:3].tolist() == [0.0, -0.09375, -0.125]
+
+
+def test_bf16_error_buffer_telescoping_up_to_storage_rounding(orc):
+    w = wl.QGZ_TINY.scaled(4 * 256 * 64)
+    e16 = np.zeros(w.R * w.N, np.uint16)
+    sum_d = np.zeros(w.R * w.N)
+    sum_g = np.zeros(w.R * w.N)
+    slack = np.zeros(w.R * w.N)
+    for t in range(4):
+        gt = wl.qgz_gradients(w, t)
+        g = wl.as_u16(gt).ravel().copy()
+        codes, scales = orc.ef_quant_int4_bf16ef(g, e16, w.N, w.R, w.G, w.B, 1.0, 0.0)
+        e_now = (e16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        sum_d += _deq(codes, scales, w.B)
+        sum_g += gt.double().numpy().ravel()
+        slack += np.abs(e_now) * 2.0**-8 + 1e-5 * (np.abs(gt.double().numpy().ravel()) + np.abs(e_now))
+    e_T = (e16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.all(np.abs(sum_d - (sum_g - e_T)) <= slack + 1e-30)
+
+
+# --------------------------------------------------------------------------
+# qwZ with the bf16 replica
+# --------------------------------------------------------------------------
+
+def test_qwz_replica_is_quantize_then_dequantize(orc):
+    w = wl.as_u16(wl.draw_bf16(2048 * 6, 0.02, 8)).copy()
+    codes, scales, rep = orc.qwz_quant_replica_int8(w, 2048)
+    c2, s2 = orc.qwz_quant_int8(w, 2048)
+    assert np.array_equal(codes, c2) and np.array_equal(scales, s2)
+    assert np.array_equal(rep, orc.qwz_dequant_int8(c2, s2, 2048))

@@ -218,3 +218,42 @@ def test_outputs_stay_inside_their_buffers(dev):
     for t, fill, n in ((efd, 13.0, R * N), (codes, 0xA5, R * N // 2), (scales, -5.0, R * N // B),
                        (c1, 0x5A, G * N // 2), (s1, -9.0, G * N // B), (out, -1.0, N)):
         assert bool((t[:pad] == fill).all()) and bool((t[pad + n:] == fill).all())
+
+
+FUSED_CASES = [
+    # R, N, B, with_ef, write_codes, out_bf16
+    (8, 8 * 256 * 13, 256, True, True, False),
+    (8, 8 * 256 * 13, 256, True, False, True),
+    (4, 4 * 512 * 5, 512, True, True, True),
+    (3, 3 * 128 * 7, 128, False, True, False),
+    (1, 1024, 1024, True, True, False),
+    (16, 16 * 256 * 2, 256, False, False, False),
+]
+
+
+@pytest.mark.parametrize("R,N,B,with_ef,write_codes,out_bf16", FUSED_CASES)
+def test_fused_step_parity(dev, R, N, B, with_ef, write_codes, out_bf16):
+    """One-kernel flat step against the oracle's two-stage definition, over
+    two chained steps (the error buffer carries over)."""
+    s, beta = 1.0, 0.5
+    ef_cpu = np.zeros(R * N, np.float32) if with_ef else None
+    efd = torch.zeros(R * N, dtype=torch.float32, device=dev) if with_ef else None
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev) if write_codes else None
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev) if write_codes else None
+    out = torch.empty(N, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
+    for t in range(2):
+        g = edge_gradients(R, N, B, seed=77 * t + R)
+        binding.qgz_step_fused(to_dev(g, dev), efd, codes, scales, out, N, R, B, s, beta, 0.5)
+        torch.cuda.synchronize()
+        cc, cs = ORC.ef_quant_int4(g, ef_cpu, N, R, 1, B, s, beta)
+        want = ORC.dequant_reduce(cc, cs, N, R, 1, B, 0.5, out_bf16)
+        if write_codes:
+            assert_bits_equal(to_host(codes), cc, f"codes step {t}")
+            assert_bits_equal(to_host(scales), cs, f"scales step {t}")
+        if with_ef:
+            assert_bits_equal(to_host(efd), ef_cpu, f"error feedback step {t}")
+        if out_bf16:
+            assert_bf16_parity(to_host(out), want, f"bf16 shards step {t}")
+        else:
+            ref = deq_magnitude(cc, cs, B).reshape(R, N).sum(0) * 0.5
+            assert_f32_parity(to_host(out), want, ref, f"fp32 shards step {t}")

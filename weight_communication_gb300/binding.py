@@ -29,6 +29,7 @@ SIGNATURES = {
     "wc_ef_quant_int4": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_dequant_reduce": [_P, _P, _I64, _I, _I, _I, _F, _P, _I, _P],
     "wc_dequant_reduce_requant": [_P, _P, _I64, _I, _I, _I, _P, _P, _P],
+    "wc_qgz_step_fused": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
     "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
     "wc_qwz_dequant_int8": [_P, _P, _P, _I64, _I, _P],
     "wc_sr_accumulate_bf16": [_P, _P, _I64, _U32, _U32, _P],
@@ -145,6 +146,26 @@ def dequant_reduce_requant(codes: torch.Tensor, scales: torch.Tensor, out_codes:
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B,
           _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
           _dev(out_scales, "out_scales", torch.float32, G * N // B, d), _stream(codes, stream))
+
+
+def qgz_step_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor | None,
+                   scales: torch.Tensor | None, out: torch.Tensor, N: int, R: int, B: int,
+                   err_scale: float = 1.0, err_beta: float = 0.0, out_scale: float = 1.0,
+                   stream=None) -> None:
+    """wc_qgz_step_fused: flat EF-quant + dequant-reduce in one kernel.
+    codes/scales (the send buffers) may both be None to skip writing them."""
+    d = g.device
+    if out.dtype == torch.float32:
+        od = WC_F32
+    elif out.dtype == torch.bfloat16:
+        od = WC_BF16
+    else:
+        raise TypeError("out must be float32 or bfloat16")
+    _call("wc_qgz_step_fused", _dev(g, "g", torch.bfloat16, R * N, d),
+          _dev(ef, "ef", torch.float32, R * N, d),
+          _dev(codes, "codes", torch.uint8, R * N // 2, d),
+          _dev(scales, "scales", torch.float32, R * N // B, d), N, R, B, err_scale, err_beta,
+          out_scale, _dev(out, "out", out.dtype, N, d), od, _stream(g, stream))
 
 
 def qwz_quant_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, B: int,

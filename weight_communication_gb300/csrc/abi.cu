@@ -41,6 +41,8 @@ int qgz_geometry(const char *fn, int64_t N, int R, int G, int B, wc::QgzGeometry
     if (N % R) return fail(WC_EINVAL, "%s: R=%d does not divide N=%lld", fn, R, (long long)N);
     const int64_t S = N / R;
     if (S % B) return fail(WC_EINVAL, "%s: B=%d does not divide the shard N/R=%lld", fn, B, (long long)S);
+    // (R*N < 2^32 with B >= 32 dividing N/R also keeps R below 65536, the
+    // grid's y limit that the reduce uses for destinations.)
     if (N >= (int64_t(1) << 32) || N * (int64_t)R >= (int64_t(1) << 32))
         return fail(WC_ERANGE, "%s: R*N = %lld must be below 2^32", fn, (long long)(N * R));
     geo->N = uint32_t(N);
@@ -119,6 +121,30 @@ WC_API int wc_dequant_reduce_requant(const uint8_t *codes, const float *scales, 
     WC_REQUIRE_PTR(fn, out_scales);
     return from_cuda(wc::launch_dequant_reduce_requant(codes, scales, out_codes, out_scales, geo,
                                                        B, static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                             int64_t N, int R, int B, float err_scale, float err_beta,
+                             float out_scale, void *out, int out_dtype, void *stream) {
+    static const char *fn = "wc_qgz_step_fused";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, 1, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (B < 128) return fail(WC_EINVAL, "%s: block B=%d must be at least 128", fn, B);
+    if (out_dtype != WC_F32 && out_dtype != WC_BF16)
+        return fail(WC_EINVAL, "%s: out_dtype %d is neither WC_F32 nor WC_BF16", fn, out_dtype);
+    if ((codes == nullptr) != (scales == nullptr))
+        return fail(WC_EINVAL, "%s: codes and scales must both be given or both be NULL", fn);
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, g);
+    WC_REQUIRE_PTR(fn, out);
+    if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
+    if (codes != nullptr && (!aligned16(codes) || !aligned16(scales)))
+        return fail(WC_EALIGN, "%s: codes or scales is not 16-byte aligned", fn);
+    return from_cuda(wc::launch_qgz_fused_step(g, ef, codes, scales, geo, B, err_scale, err_beta,
+                                               out_scale, out, out_dtype == WC_BF16,
+                                               static_cast<cudaStream_t>(stream)),
                      fn);
 }
 

@@ -11,19 +11,19 @@
 // reduce-scatter, reduction in full precision, intra-node before inter-node,
 // with kernel fusion.
 //
-// Both kernels are HBM-bound streams (about 10.5 bytes per gradient element
-// for the first, 4.6 per output element for the second).  One warp owns one
-// quantization block (or, for blocks smaller than the warp tile, each aligned
-// group of lanes owns one block), so the absmax is a warp-shuffle reduction
-// and codes, scales and the error update are produced in the same pass that
-// loads the block -- no second read, no shared memory, no block barrier.
+// One warp owns one quantization block (or, for blocks shorter than the warp
+// tile, each aligned group of lanes owns one block), so the absmax is a
+// warp-shuffle reduction and codes, scales and the error update are produced
+// in the same pass that loads the block -- no second read, no shared memory,
+// no block barrier.  Codes are rounded and unpacked with exact fp32
+// arithmetic (wc_device.cuh), never on the conversion pipe.
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
 namespace wc {
 
 // ---------------------------------------------------------------------------
-// EF compensation + int4 quantization
+// EF compensation + int4 quantization (HBM-bound: 10.5 bytes per element)
 // ---------------------------------------------------------------------------
 //
 // Lane layout: a warp tile is T = max(B, 128) consecutive gradient elements;
@@ -87,11 +87,13 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
 
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-        int q[4];
+        float q[4];
+        uint32_t packed = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) q[j] = quant_code<7>(c[k][j], bs);
-        const uint32_t packed = (uint32_t(q[0]) & 15u) | ((uint32_t(q[1]) & 15u) << 4) |
-                                ((uint32_t(q[2]) & 15u) << 8) | ((uint32_t(q[3]) & 15u) << 12);
+        for (int j = 0; j < 4; ++j) {
+            q[j] = quant_code_f<7>(c[k][j], bs);
+            packed |= (code_bits(q[j]) & 15u) << (4 * j);
+        }
         const uint32_t in_blk = B >= 128 ? 128u * k + 4u * lane : (4u * lane) % B;
         const uint32_t pos = out0 + in_blk;
         __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2), (unsigned short)packed);
@@ -152,7 +154,9 @@ cudaError_t launch_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, f
 // (g*L + l')*N + (l*G + g')*S + i for l' = 0..L-1.  Lane layout: warp tile
 // T = max(B, 256) outputs, lane t holds outputs 256*k + 8*t + j, i.e. one
 // 32-bit word of codes per source and per k: 128-byte coalesced loads and
-// stores per warp instruction.
+// stores per warp instruction.  The exact fp32 chain (one multiply and one
+// add per code, in source order) makes this kernel issue-bound rather than
+// HBM-bound at L = 8 (about 4.4 fp32/int operations per code read).
 template <int B>
 __global__ void __launch_bounds__(256)
 dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
@@ -169,6 +173,8 @@ dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
     const uint32_t tile0 = warp * uint32_t(T);
 
     const uint32_t unit_len = geo.G * geo.S;
+    const uint32_t cstride = geo.N / 2;  // bytes between consecutive ranks' codes
+    const uint32_t sstride = geo.N / B;  // scales between consecutive ranks
     float acc[K][8];
     bool active[K];
 #pragma unroll
@@ -182,11 +188,13 @@ dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
         const uint32_t i = rem - gq * geo.S;
         const uint32_t grp = u / geo.L;
         const uint32_t l = u - grp * geo.L;
-        const uint32_t base = (l * geo.G + gq) * geo.S + i;  // within a rank
+        const uint32_t pos0 = grp * geo.L * geo.N + (l * geo.G + gq) * geo.S + i;
+        const uint8_t *cp = codes + pos0 / 2;
+        const float *sp = scales + pos0 / B;
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[k][j] = 0.0f;
         if (!active[k]) continue;
-        // Loads for every source first, then the adds in source order.
+        // Loads for up to 8 sources first, then the adds in source order.
         for (uint32_t l0 = 0; l0 < geo.L; l0 += 8) {
             uint32_t w[8];
             float sc[8];
@@ -194,17 +202,18 @@ dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 if (t < nb) {
-                    const uint32_t pos = (grp * geo.L + l0 + t) * geo.N + base;
-                    w[t] = __ldg(reinterpret_cast<const uint32_t *>(codes + pos / 2));
-                    sc[t] = __ldg(scales + pos / B);
+                    w[t] = __ldcs(reinterpret_cast<const unsigned int *>(cp + (l0 + t) * cstride));
+                    sc[t] = __ldg(sp + (l0 + t) * sstride);
                 }
             }
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 if (t < nb) {
+                    float f[8];
+                    unpack_int4x8(w[t], f);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        acc[k][j] = __fadd_rn(acc[k][j], dequant(nibble(w[t], j), sc[t]));
+                        acc[k][j] = __fadd_rn(acc[k][j], dequant(f[j], sc[t]));
                 }
             }
         }
@@ -225,7 +234,7 @@ dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
         uint32_t packed = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            packed |= (uint32_t(quant_code<7>(acc[k][j], bs)) & 15u) << (4 * j);
+            packed |= (code_bits(quant_code_f<7>(acc[k][j], bs)) & 15u) << (4 * j);
         __stcs(reinterpret_cast<unsigned int *>(out_codes + o / 2), packed);
         if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
     }

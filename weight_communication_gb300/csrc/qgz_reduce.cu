@@ -13,10 +13,14 @@
 // the first-hop outputs of its L units, N elements in all), c(k) = l*G + g
 // for k = g*L + l.
 //
-// One thread makes 8 consecutive outputs: per source one 32-bit word of
-// codes (coalesced, 128 B per warp instruction) and one scale, then the 8
-// sums in source order.  Sources are fetched 8 at a time before any add so
-// that enough loads are in flight per thread.
+// Grid: y = destination, x = 8-output groups of its shard.  One thread makes
+// 8 consecutive outputs: per source one 32-bit word of codes (coalesced,
+// 128 B per warp instruction) and one scale, then the 8 sums in source
+// order.  Sources are fetched 8 at a time before any add, so that enough
+// loads are in flight per thread; the codes are unpacked with byte permutes
+// and exact fp32 subtractions (wc_device.cuh), keeping the conversion pipe
+// idle -- the per-code work is one permute, one subtract, one multiply and
+// one add.
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
@@ -27,17 +31,20 @@ __global__ void __launch_bounds__(256)
 dequant_reduce_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                       QgzGeometry geo, uint32_t nsrc, uint32_t log2_b, float out_scale,
                       void *__restrict__ out) {
+    const uint32_t k = blockIdx.y;  // destination
     const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (uint64_t(v) * 8u >= geo.N) return;
-    const uint32_t o = v * 8u;  // first output element, destination-major
-    const uint32_t k = o / geo.S;
-    const uint32_t i = o - k * geo.S;
+    if (uint64_t(v) * 8u >= geo.S) return;
+    const uint32_t i = v * 8u;  // offset in the shard
     uint32_t chunk = k;
     if (geo.G > 1) {
         const uint32_t grp = k / geo.L;
         chunk = (k - grp * geo.L) * geo.G + grp;
     }
     const uint32_t base = chunk * geo.S + i;
+    const uint8_t *cp = codes + base / 2;
+    const float *sp = scales + (base >> log2_b);
+    const uint32_t cstride = geo.N / 2;         // bytes between sources
+    const uint32_t sstride = geo.N >> log2_b;   // scales between sources
 
     float acc[8];
 #pragma unroll
@@ -49,21 +56,22 @@ dequant_reduce_kernel(const uint8_t *__restrict__ codes, const float *__restrict
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             if (t < nb) {
-                const uint32_t pos = (s0 + t) * geo.N + base;
-                w[t] = __ldcs(reinterpret_cast<const unsigned int *>(codes + pos / 2));
-                sc[t] = __ldg(scales + (pos >> log2_b));
+                w[t] = __ldcs(reinterpret_cast<const unsigned int *>(cp + (s0 + t) * cstride));
+                sc[t] = __ldg(sp + (s0 + t) * sstride);
             }
         }
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             if (t < nb) {
+                float f[8];
+                unpack_int4x8(w[t], f);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    acc[j] = __fadd_rn(acc[j], dequant(nibble(w[t], j), sc[t]));
+                for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], dequant(f[j], sc[t]));
             }
         }
     }
 
+    const uint32_t o = k * geo.S + i;
     if (OUT_BF16) {
         uint32_t h[8];
 #pragma unroll
@@ -89,8 +97,7 @@ cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
     while ((1u << log2_b) < uint32_t(B)) ++log2_b;
     const uint32_t nsrc = geo.G > 1 ? geo.G : geo.R;
     const uint32_t threads = 256;
-    const uint32_t nvec = geo.N / 8;
-    const uint32_t grid = (nvec + threads - 1) / threads;
+    const dim3 grid((geo.S / 8 + threads - 1) / threads, geo.R);
     if (out_bf16)
         dequant_reduce_kernel<true><<<grid, threads, 0, stream>>>(codes, scales, geo, nsrc,
                                                                    log2_b, out_scale, out);

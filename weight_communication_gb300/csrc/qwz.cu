@@ -10,6 +10,7 @@
 // bf16 loads and 8-byte code stores, both fully coalesced.  The raw bf16
 // words stay in registers between the absmax pass and the code pass.
 // Dequantization: one thread per 8 weights, 8-byte code load, 16-byte store.
+// Codes are rounded and unpacked with exact fp32 arithmetic (wc_device.cuh).
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
@@ -54,8 +55,8 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t half = (j & 1) ? (h[j / 2] >> 16) : (h[j / 2] & 0xFFFFu);
-            const int q = quant_code<127>(bf16_bits_to_f32(half), bs);
-            word[j / 4] |= (uint32_t(q) & 0xFFu) << (8 * (j % 4));
+            const float q = quant_code_f<127>(bf16_bits_to_f32(half), bs);
+            word[j / 4] |= (code_bits(q) & 0xFFu) << (8 * (j % 4));
         }
         __stcs(reinterpret_cast<uint2 *>(codes + x), make_uint2(word[0], word[1]));
         if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(scales + x / B, bs.scale);
@@ -70,13 +71,12 @@ qwz_dequant_int8_kernel(const int8_t *__restrict__ codes, const float *__restric
     const uint32_t x = v * 8u;
     const uint2 q = ld_stream_u2(codes + x);
     const float sc = __ldg(scales + (x >> log2_b));
-    const uint32_t qw[2] = {q.x, q.y};
+    float f[8];
+    unpack_int8x4(q.x, f);
+    unpack_int8x4(q.y, f + 4);
     uint32_t h[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int code = int(qw[j / 4] << (24 - 8 * (j % 4))) >> 24;  // sign-extend byte
-        h[j] = f32_to_bf16_bits(dequant(code, sc));
-    }
+    for (int j = 0; j < 8; ++j) h[j] = f32_to_bf16_bits(dequant(f[j], sc));
     __stcs(reinterpret_cast<uint4 *>(w_out + x),
            make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
                       h[6] | (h[7] << 16)));

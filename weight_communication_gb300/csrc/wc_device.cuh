@@ -37,18 +37,17 @@ __device__ __forceinline__ float group_max(float v) {
 }
 
 // Scale and reciprocal of a symmetric block: a block whose scale m / qmax
-// would not be a normal binary32 (m < qmax * 2^-126) is a zero block.
+// would not be a normal binary32 (m < qmax * 2^-126) is a zero block, with
+// scale 0 and inv 0 -- every finite value then quantizes to the code 0.
 struct BlockScale {
     float scale;
     float inv;
-    bool zero;
 };
 
 template <int QMAX>
 __device__ __forceinline__ BlockScale block_scale(float m) {
     BlockScale s;
-    s.zero = m < float(QMAX) * kMinNormal;  // exact product
-    if (s.zero) {
+    if (m < float(QMAX) * kMinNormal) {  // exact product
         s.scale = 0.0f;
         s.inv = 0.0f;
     } else {
@@ -58,23 +57,60 @@ __device__ __forceinline__ BlockScale block_scale(float m) {
     return s;
 }
 
-// Code of one value: clamp(rint(x * inv), -QMAX, QMAX), ties to even.
+// Integer conversions without the (slow) conversion pipe.
+//
+// Rounding: for |x| < 2^22, x + 1.5*2^23 lies in [2^23, 2^24) where the spacing
+// of binary32 is exactly 1, so the IEEE addition rounds x to the nearest
+// integer, ties to even (1.5*2^23 is even); subtracting the constant again is
+// exact.  The low bits of the sum's encoding are the integer's low bits in
+// two's complement, because the constant's low 22 bits are zero.
+constexpr float kRoundShift = 12582912.0f;  // 1.5 * 2^23
+
+__device__ __forceinline__ float round_half_even_small(float x) {
+    return __fsub_rn(__fadd_rn(x, kRoundShift), kRoundShift);
+}
+
+// Code of one value, as an exact integer-valued float:
+// clamp(rint(x * inv), -QMAX, QMAX).  (|x * inv| <= QMAX * (1 + 2^-23) for
+// every value of the block, so the clamp only guards the definition.)
 template <int QMAX>
-__device__ __forceinline__ int quant_code(float x, const BlockScale &s) {
-    if (s.zero) return 0;
-    int q = __float2int_rn(__fmul_rn(x, s.inv));
-    return min(max(q, -QMAX), QMAX);
+__device__ __forceinline__ float quant_code_f(float x, const BlockScale &s) {
+    const float q = round_half_even_small(__fmul_rn(x, s.inv));
+    return fminf(fmaxf(q, -float(QMAX)), float(QMAX));
+}
+
+// Two's-complement bits of an integer-valued float q, |q| < 2^22 (caller masks).
+__device__ __forceinline__ uint32_t code_bits(float q) {
+    return __float_as_uint(__fadd_rn(q, kRoundShift));
 }
 
 // Dequantized value: code * scale, one rounding.
-__device__ __forceinline__ float dequant(int q, float scale) {
-    return __fmul_rn(__int2float_rn(q), scale);
+__device__ __forceinline__ float dequant(float q, float scale) { return __fmul_rn(q, scale); }
+
+// Unpacking: a biased code u in [0, 2^k) placed in the mantissa of 2^23 reads
+// as 2^23 + u exactly; subtracting 2^23 + bias leaves the signed code, exact.
+// PRMT (byte permute) moves byte `b` of x under the exponent byte 0x4B.
+__device__ __forceinline__ float biased_byte_to_float(uint32_t x, int b, float offset) {
+    return __fsub_rn(__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u + b)), offset);
 }
 
-// Signed value of nibble j (0..7) of a packed 32-bit word (element 2k in the
-// low nibble of byte k).
-__device__ __forceinline__ int nibble(uint32_t w, int j) {
-    return int(w << (28 - 4 * j)) >> 28;  // arithmetic shift sign-extends
+// The 8 signed int4 codes of a packed word (element 2k in the low nibble of
+// byte k), as exact floats.
+__device__ __forceinline__ void unpack_int4x8(uint32_t w, float f[8]) {
+    const uint32_t lo = (w ^ 0x88888888u) & 0x0F0F0F0Fu;         // nibble + 8, even elements
+    const uint32_t hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;  // nibble + 8, odd elements
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        f[2 * b] = biased_byte_to_float(lo, b, 8388616.0f);      // 2^23 + 8
+        f[2 * b + 1] = biased_byte_to_float(hi, b, 8388616.0f);
+    }
+}
+
+// The 4 signed int8 codes of a packed word, as exact floats.
+__device__ __forceinline__ void unpack_int8x4(uint32_t w, float f[4]) {
+    const uint32_t u = w ^ 0x80808080u;                            // byte + 128
+#pragma unroll
+    for (int b = 0; b < 4; ++b) f[b] = biased_byte_to_float(u, b, 8388736.0f);  // 2^23 + 128
 }
 
 // Streaming (read-once) and plain vector accesses.

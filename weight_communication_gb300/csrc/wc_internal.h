@@ -28,6 +28,10 @@ cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
 cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *scales,
                                           uint8_t *out_codes, float *out_scales,
                                           const QgzGeometry &geo, int B, cudaStream_t stream);
+cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                                  const QgzGeometry &geo, int B, float s, float beta,
+                                  float out_scale, void *out, bool out_bf16,
+                                  cudaStream_t stream);
 cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, uint32_t n,
                                   int B, cudaStream_t stream);
 cudaError_t launch_qwz_dequant_int8(const int8_t *codes, const float *scales, uint16_t *w_out,
