@@ -99,6 +99,21 @@ WC_API int wc_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes,
                             float err_scale, float err_beta, void *stream);
 
 /*
+ * wc_ef_quant_int4_bf16ef -- wc_ef_quant_int4 with the error buffer stored in
+ * bf16 instead of fp32, halving the extra memory LoCo costs ("Merge LoCo with
+ * Zero++", Overview) and the buffer's share of the traffic (6.5 instead of
+ * 10.5 bytes per element at B = 256).  The stored error is widened exactly,
+ * all arithmetic is the fp32 chain of wc_ef_quant_int4, and only the new
+ * error is rounded to the nearest bf16 (ties to even) when stored.
+ * ef16 : [R][N] bf16 bit patterns, read and written in place (not NULL).
+ * Everything else as wc_ef_quant_int4.
+ */
+WC_API int wc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *ef16,
+                                   uint8_t *codes, float *scales, int64_t N,
+                                   int R, int G, int B, float err_scale,
+                                   float err_beta, void *stream);
+
+/*
  * wc_dequant_reduce -- dequantize and reduce in full precision (steps a6-a7,
  * and a9 for the second hop of the hierarchical reduce).
  *
@@ -175,6 +190,19 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes,
  */
 WC_API int wc_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
                              int64_t n, int B, void *stream);
+
+/*
+ * wc_qwz_quant_replica_int8 -- wc_qwz_quant_int8 that also writes, in the same
+ * pass, the bf16 weights the codes stand for: replica = bf16_rn(q * scale),
+ * exactly what wc_qwz_dequant_int8 returns for these codes.  This is the
+ * copy a node keeps after the quantized forward all-gather ("ZeROPlusPlus.md"
+ * §1.2: the hierarchical partition keeps a full model copy inside each node),
+ * written without re-reading the codes: 5 bytes per weight instead of 6.
+ * replica : [n] bf16, written.  Everything else as wc_qwz_quant_int8.
+ */
+WC_API int wc_qwz_quant_replica_int8(const uint16_t *w, int8_t *codes,
+                                     float *scales, uint16_t *replica,
+                                     int64_t n, int B, void *stream);
 
 /*
  * wc_qwz_dequant_int8 -- back to bf16 (step a11): w' = bf16_rn(q * scale).

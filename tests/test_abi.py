@@ -138,3 +138,15 @@ def test_fused_step_argument_errors(lib):
     assert call(ef=MIS) == binding.WC_EALIGN
     assert call(g=None) == binding.WC_EINVAL
     assert call(N=0, g=None, out=None) == binding.WC_OK
+
+
+def test_bf16ef_and_replica_argument_errors(lib):
+    f = lib.wc_ef_quant_int4_bf16ef
+    assert f(FAKE, None, FAKE, FAKE, 1024, 4, 1, 256, 1.0, 0.5, None) == binding.WC_EINVAL
+    assert f(FAKE, MIS, FAKE, FAKE, 1024, 4, 1, 256, 1.0, 0.5, None) == binding.WC_EALIGN
+    assert f(FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 100, 1.0, 0.5, None) == binding.WC_EINVAL
+    assert f(None, None, None, None, 0, 4, 1, 256, 1.0, 0.5, None) == binding.WC_OK
+    q = lib.wc_qwz_quant_replica_int8
+    assert q(FAKE, FAKE, FAKE, None, 4096, 2048, None) == binding.WC_EINVAL
+    assert q(FAKE, FAKE, FAKE, MIS, 4096, 2048, None) == binding.WC_EALIGN
+    assert q(FAKE, FAKE, FAKE, FAKE, 4000, 2048, None) == binding.WC_EINVAL

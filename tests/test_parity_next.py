@@ -1,0 +1,85 @@
+"""GPU parity (through the C ABI) of the entry points beyond the basic path,
+against the CPU oracle:
+
+  * wc_ef_quant_int4_bf16ef -- EF-quant with a bf16 error buffer, over
+    chained steps, every block size and grouped send orders;
+  * wc_qwz_quant_replica_int8 -- qwZ quantization writing the bf16 replica.
+
+The fused flat step's parity is in test_parity_qgz.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_bits_equal, dev, to_dev, to_host
+from test_parity_qgz import edge_gradients
+from test_parity_secondary import weights_with_edges
+from weight_communication_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+ORC = oracle.get()
+
+BF16EF_CASES = [
+    # R, N, G, B, s, beta
+    (8, 8 * 256 * 9, 1, 256, 1.0, 0.5),
+    (4, 4 * 256 * 5, 1, 256, 1.0, 0.0),
+    (16, 16 * 512 * 2, 2, 512, 1.0, 0.5),
+    (6, 6 * 64 * 11, 3, 64, 0.75, 0.25),
+    (2, 2 * 32 * 9, 1, 32, 2.0, 0.5),
+    (3, 3 * 1024, 1, 1024, 1.0, 0.5),
+]
+
+
+@pytest.mark.parametrize("R,N,G,B,s,beta", BF16EF_CASES)
+def test_bf16_error_buffer_parity(dev, R, N, G, B, s, beta):
+    rng = np.random.default_rng(N + B)
+    e0 = wl.as_u16(torch.from_numpy((rng.standard_normal(R * N) * 1e-4).astype(np.float32))
+                   .to(torch.bfloat16)).copy()
+    e_cpu = e0.copy()
+    e_dev = to_dev(e0, dev)
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    for t in range(3):
+        g = edge_gradients(R, N, B, seed=13 * t + R + B)
+        binding.ef_quant_int4_bf16ef(to_dev(g, dev), e_dev, codes, scales, N, R, G, B, s, beta)
+        torch.cuda.synchronize()
+        cc, cs = ORC.ef_quant_int4_bf16ef(g, e_cpu, N, R, G, B, s, beta)
+        assert_bits_equal(to_host(codes), cc, f"codes step {t}")
+        assert_bits_equal(to_host(scales), cs, f"scales step {t}")
+        assert_bits_equal(to_host(e_dev), e_cpu, f"bf16 error step {t}")
+
+
+def test_bf16_error_buffer_full_size(dev):
+    """Single-hop workload size, two chained steps, every output."""
+    w = wl.QGZ_SINGLE_HOP
+    e_dev = torch.zeros(w.R * w.N, dtype=torch.bfloat16, device=dev)
+    e_cpu = np.zeros(w.R * w.N, np.uint16)
+    codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+    gd = torch.empty((w.R, w.N), dtype=torch.bfloat16, device=dev)
+    for t in range(2):
+        wl.qgz_gradients(w, t, device=dev, out=gd)
+        binding.ef_quant_int4_bf16ef(gd.view(-1), e_dev, codes, scales, w.N, w.R, 1, w.B,
+                                     w.err_scale, w.err_beta)
+        torch.cuda.synchronize()
+        cc, cs = ORC.ef_quant_int4_bf16ef(to_host(gd).ravel(), e_cpu, w.N, w.R, 1, w.B,
+                                          w.err_scale, w.err_beta)
+        assert_bits_equal(to_host(codes), cc, f"codes step {t}")
+        assert_bits_equal(to_host(scales), cs, f"scales step {t}")
+        assert_bits_equal(to_host(e_dev), e_cpu, f"bf16 error step {t}")
+
+
+@pytest.mark.parametrize("n,B", [(2048 * 21, 2048), (256 * 33, 256), (32 * 13, 32), (4096 * 2, 4096)])
+def test_qwz_replica_parity(dev, n, B):
+    w = weights_with_edges(n, B, seed=3 * n + B)
+    codes = torch.empty(n, dtype=torch.int8, device=dev)
+    scales = torch.empty(n // B, dtype=torch.float32, device=dev)
+    rep = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    binding.qwz_quant_replica_int8(to_dev(w, dev), codes, scales, rep, B)
+    torch.cuda.synchronize()
+    oc, os_, orep = ORC.qwz_quant_replica_int8(w, B)
+    assert_bits_equal(to_host(codes), oc, "codes")
+    assert_bits_equal(to_host(scales), os_, "scales")
+    assert_bits_equal(to_host(rep), orep, "replica")

@@ -30,7 +30,9 @@ SIGNATURES = {
     "wc_dequant_reduce": [_P, _P, _I64, _I, _I, _I, _F, _P, _I, _P],
     "wc_dequant_reduce_requant": [_P, _P, _I64, _I, _I, _I, _P, _P, _P],
     "wc_qgz_step_fused": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
+    "wc_ef_quant_int4_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
+    "wc_qwz_quant_replica_int8": [_P, _P, _P, _P, _I64, _I, _P],
     "wc_qwz_dequant_int8": [_P, _P, _P, _I64, _I, _P],
     "wc_sr_accumulate_bf16": [_P, _P, _I64, _U32, _U32, _P],
     "wc_last_error": [],
@@ -175,6 +177,28 @@ def qwz_quant_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, B
     _call("wc_qwz_quant_int8", _dev(w, "w", torch.bfloat16, n, d),
           _dev(codes, "codes", torch.int8, n, d), _dev(scales, "scales", torch.float32, n // B, d),
           n, B, _stream(w, stream))
+
+
+def ef_quant_int4_bf16ef(g: torch.Tensor, ef16: torch.Tensor, codes: torch.Tensor,
+                         scales: torch.Tensor, N: int, R: int, G: int, B: int,
+                         err_scale: float = 1.0, err_beta: float = 0.0, stream=None) -> None:
+    """wc_ef_quant_int4_bf16ef: as ef_quant_int4 with a bf16 error buffer."""
+    d = g.device
+    _call("wc_ef_quant_int4_bf16ef", _dev(g, "g", torch.bfloat16, R * N, d),
+          _dev(ef16, "ef16", torch.bfloat16, R * N, d),
+          _dev(codes, "codes", torch.uint8, R * N // 2, d),
+          _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
+          _stream(g, stream))
+
+
+def qwz_quant_replica_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                           replica: torch.Tensor, B: int, stream=None) -> None:
+    """wc_qwz_quant_replica_int8: codes, scales and the bf16 replica in one pass."""
+    n = w.numel()
+    d = w.device
+    _call("wc_qwz_quant_replica_int8", _dev(w, "w", torch.bfloat16, n, d),
+          _dev(codes, "codes", torch.int8, n, d), _dev(scales, "scales", torch.float32, n // B, d),
+          _dev(replica, "replica", torch.bfloat16, n, d), n, B, _stream(w, stream))
 
 
 def qwz_dequant_int8(codes: torch.Tensor, scales: torch.Tensor, w_out: torch.Tensor, B: int,

@@ -81,8 +81,25 @@ WC_API int wc_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float 
     WC_REQUIRE_PTR(fn, codes);
     WC_REQUIRE_PTR(fn, scales);
     if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
-    return from_cuda(wc::launch_ef_quant_int4(g, ef, codes, scales, geo, B, err_scale, err_beta,
-                                              static_cast<cudaStream_t>(stream)),
+    return from_cuda(wc::launch_ef_quant_int4(g, ef, false, codes, scales, geo, B, err_scale,
+                                              err_beta, static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *ef16, uint8_t *codes,
+                                   float *scales, int64_t N, int R, int G, int B,
+                                   float err_scale, float err_beta, void *stream) {
+    static const char *fn = "wc_ef_quant_int4_bf16ef";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, g);
+    WC_REQUIRE_PTR(fn, ef16);
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    return from_cuda(wc::launch_ef_quant_int4(g, ef16, true, codes, scales, geo, B, err_scale,
+                                              err_beta, static_cast<cudaStream_t>(stream)),
                      fn);
 }
 
@@ -166,7 +183,22 @@ WC_API int wc_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, in
     WC_REQUIRE_PTR(fn, w);
     WC_REQUIRE_PTR(fn, codes);
     WC_REQUIRE_PTR(fn, scales);
-    return from_cuda(wc::launch_qwz_quant_int8(w, codes, scales, uint32_t(n), B,
+    return from_cuda(wc::launch_qwz_quant_int8(w, codes, scales, nullptr, uint32_t(n), B,
+                                               static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_qwz_quant_replica_int8(const uint16_t *w, int8_t *codes, float *scales,
+                                     uint16_t *replica, int64_t n, int B, void *stream) {
+    static const char *fn = "wc_qwz_quant_replica_int8";
+    int rc = qwz_sizes(fn, n, B);
+    if (rc != WC_OK) return rc;
+    if (n == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, w);
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    WC_REQUIRE_PTR(fn, replica);
+    return from_cuda(wc::launch_qwz_quant_int8(w, codes, scales, replica, uint32_t(n), B,
                                                static_cast<cudaStream_t>(stream)),
                      fn);
 }

@@ -30,11 +30,19 @@ namespace wc {
 // lane t holds elements 128*k + 4*t + j (k < T/128, j < 4).  Every access is
 // then fully coalesced: 8-byte bf16 loads (256 B per warp instruction),
 // 16-byte fp32 error loads and stores (512 B), 2-byte code stores (64 B).
-template <int B, bool HAS_EF>
+//
+// EF selects the error buffer: none, fp32 (4 bytes per element each way) or
+// bf16 (2 bytes; the new error is rounded to the nearest bf16 when stored).
+enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2 };
+
+template <int B, int EF>
 __global__ void __launch_bounds__(256)
-ef_quant_int4_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
+ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                      uint8_t *__restrict__ codes, float *__restrict__ scales,
                      QgzGeometry geo, float s, float beta, float one_minus_beta) {
+    constexpr bool HAS_EF = EF != kEfNone;
+    float *__restrict__ ef = static_cast<float *>(ef_v);
+    uint16_t *__restrict__ ef16 = static_cast<uint16_t *>(ef_v);
     constexpr int T = B >= 128 ? B : 128;
     constexpr int K = T / 128;
     constexpr int LPB = B >= 128 ? 32 : B / 4;  // lanes per block
@@ -66,7 +74,12 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
         float4 ev = make_float4(0.f, 0.f, 0.f, 0.f);
         if (active) {
             gv = ld_stream_u2(g + x);
-            if (HAS_EF) ev = ld_stream_f4(ef + x);
+            if (EF == kEfF32) ev = ld_stream_f4(ef + x);
+            if (EF == kEfBf16) {
+                const uint2 eh = ld_stream_u2(ef16 + x);
+                ev = make_float4(bf16_bits_to_f32(eh.x & 0xFFFFu), bf16_bits_to_f32(eh.x >> 16),
+                                 bf16_bits_to_f32(eh.y & 0xFFFFu), bf16_bits_to_f32(eh.y >> 16));
+            }
         }
         const float gf[4] = {bf16_bits_to_f32(gv.x & 0xFFFFu), bf16_bits_to_f32(gv.x >> 16),
                              bf16_bits_to_f32(gv.y & 0xFFFFu), bf16_bits_to_f32(gv.y >> 16)};
@@ -107,14 +120,18 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
                                  __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));
             }
             const uint32_t x = tile0 + 128u * k + 4u * lane;
-            __stcs(reinterpret_cast<float4 *>(ef + x), ev);
+            if (EF == kEfF32) __stcs(reinterpret_cast<float4 *>(ef + x), ev);
+            if (EF == kEfBf16)
+                __stcs(reinterpret_cast<uint2 *>(ef16 + x),
+                       make_uint2(uint32_t(f32_to_bf16_bits(ev.x)) | (uint32_t(f32_to_bf16_bits(ev.y)) << 16),
+                                  uint32_t(f32_to_bf16_bits(ev.z)) | (uint32_t(f32_to_bf16_bits(ev.w)) << 16)));
         }
     }
     if ((lane & (LPB - 1)) == 0) __stcs(scales + out0 / B, bs.scale);
 }
 
 template <int B>
-static cudaError_t launch_ef_quant_b(const uint16_t *g, float *ef, uint8_t *codes,
+static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
                                      float *scales, const QgzGeometry &geo, float s,
                                      float beta, cudaStream_t stream) {
     constexpr int T = B >= 128 ? B : 128;
@@ -122,25 +139,28 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, float *ef, uint8_t *code
     const uint32_t threads = 256;
     const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
     const float omb = 1.0f - beta;
-    if (ef)
-        ef_quant_int4_kernel<B, true><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
-                                                                     s, beta, omb);
+    if (ef == nullptr)
+        ef_quant_int4_kernel<B, kEfNone><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
+                                                                        s, beta, omb);
+    else if (ef_bf16)
+        ef_quant_int4_kernel<B, kEfBf16><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
+                                                                        s, beta, omb);
     else
-        ef_quant_int4_kernel<B, false><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
-                                                                      s, beta, omb);
+        ef_quant_int4_kernel<B, kEfF32><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
+                                                                       s, beta, omb);
     return cudaPeekAtLastError();
 }
 
-cudaError_t launch_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
-                                 const QgzGeometry &geo, int B, float s, float beta,
-                                 cudaStream_t stream) {
+cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
+                                 float *scales, const QgzGeometry &geo, int B, float s,
+                                 float beta, cudaStream_t stream) {
     switch (B) {
-        case 32: return launch_ef_quant_b<32>(g, ef, codes, scales, geo, s, beta, stream);
-        case 64: return launch_ef_quant_b<64>(g, ef, codes, scales, geo, s, beta, stream);
-        case 128: return launch_ef_quant_b<128>(g, ef, codes, scales, geo, s, beta, stream);
-        case 256: return launch_ef_quant_b<256>(g, ef, codes, scales, geo, s, beta, stream);
-        case 512: return launch_ef_quant_b<512>(g, ef, codes, scales, geo, s, beta, stream);
-        case 1024: return launch_ef_quant_b<1024>(g, ef, codes, scales, geo, s, beta, stream);
+        case 32: return launch_ef_quant_b<32>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
+        case 64: return launch_ef_quant_b<64>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
+        case 128: return launch_ef_quant_b<128>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
+        case 256: return launch_ef_quant_b<256>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
+        case 512: return launch_ef_quant_b<512>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
+        case 1024: return launch_ef_quant_b<1024>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
         default: return cudaErrorInvalidValue;
     }
 }

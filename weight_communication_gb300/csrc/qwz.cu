@@ -16,10 +16,12 @@
 
 namespace wc {
 
-template <int B>
+// REPLICA also writes the bf16 weights the codes stand for, bf16_rn(q*scale),
+// in the same pass (the dequantized copy a node keeps).
+template <int B, bool REPLICA>
 __global__ void __launch_bounds__(256)
 qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes,
-                      float *__restrict__ scales, uint32_t n) {
+                      float *__restrict__ scales, uint16_t *__restrict__ replica, uint32_t n) {
     constexpr int T = B >= 256 ? B : 256;
     constexpr int K = T / 256;
     constexpr int LPB = B >= 256 ? 32 : B / 8;
@@ -52,13 +54,18 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
         const uint32_t x = tile0 + 256u * k + 8u * lane;
         const uint32_t *h = &raw[k].x;
         uint32_t word[2] = {0u, 0u};
+        uint32_t rep[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t half = (j & 1) ? (h[j / 2] >> 16) : (h[j / 2] & 0xFFFFu);
             const float q = quant_code_f<127>(bf16_bits_to_f32(half), bs);
             word[j / 4] |= (code_bits(q) & 0xFFu) << (8 * (j % 4));
+            if (REPLICA)
+                rep[j / 2] |= uint32_t(f32_to_bf16_bits(dequant(q, bs.scale))) << (16 * (j & 1));
         }
         __stcs(reinterpret_cast<uint2 *>(codes + x), make_uint2(word[0], word[1]));
+        if (REPLICA)
+            __stcs(reinterpret_cast<uint4 *>(replica + x), make_uint4(rep[0], rep[1], rep[2], rep[3]));
         if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(scales + x / B, bs.scale);
     }
 }
@@ -84,26 +91,29 @@ qwz_dequant_int8_kernel(const int8_t *__restrict__ codes, const float *__restric
 
 template <int B>
 static cudaError_t launch_qwz_quant_b(const uint16_t *w, int8_t *codes, float *scales,
-                                      uint32_t n, cudaStream_t stream) {
+                                      uint16_t *replica, uint32_t n, cudaStream_t stream) {
     constexpr int T = B >= 256 ? B : 256;
     const uint32_t tiles = (n + T - 1) / T;
     const uint32_t threads = 256;
     const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
-    qwz_quant_int8_kernel<B><<<grid, threads, 0, stream>>>(w, codes, scales, n);
+    if (replica)
+        qwz_quant_int8_kernel<B, true><<<grid, threads, 0, stream>>>(w, codes, scales, replica, n);
+    else
+        qwz_quant_int8_kernel<B, false><<<grid, threads, 0, stream>>>(w, codes, scales, replica, n);
     return cudaPeekAtLastError();
 }
 
-cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, uint32_t n,
-                                  int B, cudaStream_t stream) {
+cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
+                                  uint16_t *replica, uint32_t n, int B, cudaStream_t stream) {
     switch (B) {
-        case 32: return launch_qwz_quant_b<32>(w, codes, scales, n, stream);
-        case 64: return launch_qwz_quant_b<64>(w, codes, scales, n, stream);
-        case 128: return launch_qwz_quant_b<128>(w, codes, scales, n, stream);
-        case 256: return launch_qwz_quant_b<256>(w, codes, scales, n, stream);
-        case 512: return launch_qwz_quant_b<512>(w, codes, scales, n, stream);
-        case 1024: return launch_qwz_quant_b<1024>(w, codes, scales, n, stream);
-        case 2048: return launch_qwz_quant_b<2048>(w, codes, scales, n, stream);
-        case 4096: return launch_qwz_quant_b<4096>(w, codes, scales, n, stream);
+        case 32: return launch_qwz_quant_b<32>(w, codes, scales, replica, n, stream);
+        case 64: return launch_qwz_quant_b<64>(w, codes, scales, replica, n, stream);
+        case 128: return launch_qwz_quant_b<128>(w, codes, scales, replica, n, stream);
+        case 256: return launch_qwz_quant_b<256>(w, codes, scales, replica, n, stream);
+        case 512: return launch_qwz_quant_b<512>(w, codes, scales, replica, n, stream);
+        case 1024: return launch_qwz_quant_b<1024>(w, codes, scales, replica, n, stream);
+        case 2048: return launch_qwz_quant_b<2048>(w, codes, scales, replica, n, stream);
+        case 4096: return launch_qwz_quant_b<4096>(w, codes, scales, replica, n, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -19,9 +19,10 @@ struct QgzGeometry {
     uint32_t total;            // R * N
 };
 
-cudaError_t launch_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
-                                 const QgzGeometry &geo, int B, float s, float beta,
-                                 cudaStream_t stream);
+// ef: fp32 [R][N], bf16 [R][N] (ef_bf16) or NULL.
+cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
+                                 float *scales, const QgzGeometry &geo, int B, float s,
+                                 float beta, cudaStream_t stream);
 cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
                                   const QgzGeometry &geo, int B, float out_scale, void *out,
                                   bool out_bf16, cudaStream_t stream);
@@ -32,8 +33,9 @@ cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, 
                                   const QgzGeometry &geo, int B, float s, float beta,
                                   float out_scale, void *out, bool out_bf16,
                                   cudaStream_t stream);
-cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales, uint32_t n,
-                                  int B, cudaStream_t stream);
+// replica: bf16 [n] written with the dequantized weights, or NULL.
+cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
+                                  uint16_t *replica, uint32_t n, int B, cudaStream_t stream);
 cudaError_t launch_qwz_dequant_int8(const int8_t *codes, const float *scales, uint16_t *w_out,
                                     uint32_t n, int B, cudaStream_t stream);
 cudaError_t launch_sr_accumulate(uint16_t *dst, uint16_t *src, uint32_t n, uint32_t seed,

@@ -30,13 +30,17 @@ class QgzReducer:
 
     def __init__(self, N: int, R: int, G: int = 1, B: int = 256, err_scale: float = 1.0,
                  err_beta: float = 0.0, use_ef: bool = True, out_dtype=torch.float32,
-                 out_scale: float = 1.0, device="cuda"):
+                 out_scale: float = 1.0, device="cuda", ef_dtype=torch.float32):
+        """ef_dtype: torch.float32, or torch.bfloat16 for the half-size error
+        buffer (wc_ef_quant_int4_bf16ef)."""
         self.N, self.R, self.G, self.B = N, R, G, B
         self.err_scale, self.err_beta = err_scale, err_beta
         self.out_scale = out_scale
         self.device = torch.device(device)
         dev = self.device
-        self.ef = torch.zeros(R * N, dtype=torch.float32, device=dev) if use_ef else None
+        if ef_dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("ef_dtype must be float32 or bfloat16")
+        self.ef = torch.zeros(R * N, dtype=ef_dtype, device=dev) if use_ef else None
         self.codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
         self.scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
         if G > 1:
@@ -51,8 +55,13 @@ class QgzReducer:
         return 3 if self.G > 1 else 2
 
     def quantize(self, g: torch.Tensor, stream=None) -> None:
-        binding.ef_quant_int4(g.reshape(-1), self.ef, self.codes, self.scales, self.N, self.R,
-                              self.G, self.B, self.err_scale, self.err_beta, stream)
+        if self.ef is not None and self.ef.dtype == torch.bfloat16:
+            binding.ef_quant_int4_bf16ef(g.reshape(-1), self.ef, self.codes, self.scales, self.N,
+                                         self.R, self.G, self.B, self.err_scale, self.err_beta,
+                                         stream)
+        else:
+            binding.ef_quant_int4(g.reshape(-1), self.ef, self.codes, self.scales, self.N, self.R,
+                                  self.G, self.B, self.err_scale, self.err_beta, stream)
 
     def reduce(self, stream=None) -> torch.Tensor:
         if self.G > 1:
