@@ -252,10 +252,13 @@ class Timer:
         return statistics.mean(e[0].elapsed_time(e[-1]) for e in self.ev)
 
 
-def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws):
+def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False):
+    """One qgZ step per timed iteration; ef_bf16 keeps the error buffer in
+    bf16 (wc_ef_quant_int4_bf16ef) instead of fp32."""
     from weight_communication_gb300.qgz import QgzReducer
     out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
-    red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev)
+    red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                     ef_dtype=torch.bfloat16 if ef_bf16 else torch.float32)
     g_bytes = w.R * w.N * 2
     nbatch = max(1, min(args.batches, (8 << 30) // g_bytes))
     batches = [wl.qgz_gradients(w, t, device=dev) for t in range(nbatch)]
@@ -317,10 +320,12 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws):
 
     # roofline of the dominant kernel (the error-feedback quantization)
     peak, peak_kind = measured_peaks()
-    efq_bytes = w.R * w.N * (2 + 4 + 4 + 0.5) + w.R * w.N // w.B * 4
+    ef_bytes = 2 if ef_bf16 else 4
+    efq_bytes = w.R * w.N * (2 + 2 * ef_bytes + 0.5) + w.R * w.N // w.B * 4
     efq_ms = per_kernel["ef_quant_int4"]
     achieved = efq_bytes / (efq_ms / 1e3) / 1e9
-    traffic = ncu_traffic("ef_quant_int4", w.name.split()[0], units)
+    efq_kernel = "ef_quant_int4_bf16ef" if ef_bf16 else "ef_quant_int4"
+    traffic = ncu_traffic(efq_kernel, w.name.split()[0], units) if not ef_bf16 else None
     kernels = {}
     S = w.S
     for n in names:
@@ -340,13 +345,15 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded normal gradients with sparse outliers)",
-        "config": {"workload": w.name, "R": w.R, "N": w.N, "G": w.G, "B": w.B,
+        "config": {"workload": w.name + (" bf16 error buffer" if ef_bf16 else ""),
+                   "R": w.R, "N": w.N, "G": w.G, "B": w.B,
                    "err_scale": w.err_scale, "err_beta": w.err_beta,
+                   "ef": "bf16" if ef_bf16 else "fp32",
                    "out": "bf16" if w.out_bf16 else "fp32",
                    "l2": ("flushed between steps (untimed 516 MB write)" if flush is not None
                           else f"inputs exceed L2 ({units * 10 / 1e9:.1f} GB per step)"),
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": "ef_quant_int4", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": efq_kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": int(efq_bytes)},
@@ -460,13 +467,28 @@ def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
             timer.mark(i, 2)
         torch.cuda.synchronize(dev)
         barrier(dist)
+    # the one-pass variant that writes the codes and the bf16 replica, timed
+    # on its own (not part of the round-trip step)
+    rep_steps = max(1, min(args.steps, 200))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            binding.qwz_quant_replica_int8(wd, codes, scales, back, w.B, stream)
+        rtimer = Timer(["qwz_quant_replica_int8"], rep_steps)
+        for i in range(rep_steps):
+            rtimer.mark(i, 0)
+            binding.qwz_quant_replica_int8(wd, codes, scales, back, w.B, stream)
+            rtimer.mark(i, 1)
+        torch.cuda.synchronize(dev)
     per = timer.per_kernel_ms()
+    per.update(rtimer.per_kernel_ms())
     ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
     peak, kind = measured_peaks()
     qb = w.n * (2 + 1) + w.n // w.B * 4
-    kernels = {n: {"ms": round(per[n], 5), "algorithmic_bytes": qb,
-                   "GB/s": round(qb / (per[n] / 1e3) / 1e9, 1),
-                   "frac": round(qb / (per[n] / 1e3) / 1e9 / peak, 4)} for n in names}
+    kb = {"qwz_quant_int8": qb, "qwz_dequant_int8": qb,
+          "qwz_quant_replica_int8": qb + 2 * w.n}
+    kernels = {n: {"ms": round(per[n], 5), "algorithmic_bytes": kb[n],
+                   "GB/s": round(kb[n] / (per[n] / 1e3) / 1e9, 1),
+                   "frac": round(kb[n] / (per[n] / 1e3) / 1e9 / peak, 4)} for n in kb}
     return {"metric": "qwZ weights/s (int8 quantize + dequantize round trip)",
             "value": w.n * ws / (ms / 1e3), "unit": "weights/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -620,8 +642,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
-                    choices=["qgz_single_hop", "qgz_fused", "qgz_tiny", "qgz_hierarchical",
-                             "qwz", "sr", "all"])
+                    choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_tiny",
+                             "qgz_hierarchical", "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
@@ -648,10 +670,13 @@ def main(argv=None):
     from weight_communication_gb300 import binding
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
-    names = (["qgz_single_hop", "qgz_fused", "qgz_tiny", "qgz_hierarchical", "qwz", "sr"]
-             if args.workload == "all" else [args.workload])
+    names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_tiny", "qgz_hierarchical", "qwz",
+              "sr"] if args.workload == "all" else [args.workload])
     for name in names:
-        if name == "qgz_fused":
+        if name == "qgz_bf16ef":
+            w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
+            line, _ = run_qgz(w, args, dev, dist, ws, ef_bf16=True)
+        elif name == "qgz_fused":
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
             line, _ = run_qgz_fused(w, args, dev, dist, ws)
         elif name in wl.QGZ_WORKLOADS:
