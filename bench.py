@@ -187,7 +187,7 @@ KERNEL_SOURCES = {
                       "weight_communication_gb300/csrc/wc_device.cuh"],
     "dequant_reduce": ["weight_communication_gb300/csrc/qgz_reduce.cu",
                        "weight_communication_gb300/csrc/wc_device.cuh"],
-    "dequant_reduce_requant": ["weight_communication_gb300/csrc/qgz_quant.cu",
+    "dequant_reduce_requant": ["weight_communication_gb300/csrc/qgz_hop1.cu",
                                "weight_communication_gb300/csrc/wc_device.cuh"],
     "qwz_quant_int8": ["weight_communication_gb300/csrc/qwz.cu",
                        "weight_communication_gb300/csrc/wc_device.cuh"],
@@ -252,13 +252,15 @@ class Timer:
         return statistics.mean(e[0].elapsed_time(e[-1]) for e in self.ev)
 
 
-def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False):
+def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
+            hop1_ef: bool = False):
     """One qgZ step per timed iteration; ef_bf16 keeps the error buffer in
-    bf16 (wc_ef_quant_int4_bf16ef) instead of fp32."""
+    bf16 (wc_ef_quant_int4_bf16ef) instead of fp32; hop1_ef adds error
+    feedback to the first hop's requantization (hierarchical only)."""
     from weight_communication_gb300.qgz import QgzReducer
     out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
     red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
-                     ef_dtype=torch.bfloat16 if ef_bf16 else torch.float32)
+                     ef_dtype=torch.bfloat16 if ef_bf16 else torch.float32, hop1_ef=hop1_ef)
     g_bytes = w.R * w.N * 2
     nbatch = max(1, min(args.batches, (8 << 30) // g_bytes))
     batches = [wl.qgz_gradients(w, t, device=dev) for t in range(nbatch)]
@@ -275,15 +277,10 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False):
         if timer is not None:
             timer.mark(ti, 1)
         if w.G > 1:
-            from weight_communication_gb300 import binding
-            binding.dequant_reduce_requant(red.codes, red.scales, red.codes1, red.scales1,
-                                           w.N, w.R, w.G, w.B, stream)
+            red.reduce_first_hop(stream)
             if timer is not None:
                 timer.mark(ti, 2)
-            binding.dequant_reduce(red.codes1, red.scales1, red.out, w.N, w.R, w.G, w.B, 1.0, stream)
-        else:
-            from weight_communication_gb300 import binding
-            binding.dequant_reduce(red.codes, red.scales, red.out, w.N, w.R, 1, w.B, 1.0, stream)
+        red.reduce_last_hop(stream)
         if timer is not None:
             timer.mark(ti, len(names))
 
@@ -332,7 +329,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False):
         if n == "ef_quant_int4":
             b = efq_bytes
         elif n == "dequant_reduce_requant":
-            b = w.G * w.N * (w.L + 1) * (0.5 + 4 / w.B)
+            b = w.G * w.N * (w.L + 1) * (0.5 + 4 / w.B) + (8 * w.G * w.N if hop1_ef else 0)
         else:
             nsrc = w.G if w.G > 1 else w.R
             b = w.N * (nsrc * (0.5 + 4 / w.B) + (2 if w.out_bf16 else 4))
@@ -345,7 +342,8 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded normal gradients with sparse outliers)",
-        "config": {"workload": w.name + (" bf16 error buffer" if ef_bf16 else ""),
+        "config": {"workload": w.name + (" bf16 error buffer" if ef_bf16 else "")
+                   + (" + first-hop error feedback" if hop1_ef else ""),
                    "R": w.R, "N": w.N, "G": w.G, "B": w.B,
                    "err_scale": w.err_scale, "err_beta": w.err_beta,
                    "ef": "bf16" if ef_bf16 else "fp32",
@@ -642,7 +640,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
-                    choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_tiny",
+                    choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_hier_ef", "qgz_tiny",
                              "qgz_hierarchical", "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -670,10 +668,14 @@ def main(argv=None):
     from weight_communication_gb300 import binding
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
-    names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_tiny", "qgz_hierarchical", "qwz",
+    names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_tiny", "qgz_hierarchical",
+              "qgz_hier_ef", "qwz",
               "sr"] if args.workload == "all" else [args.workload])
     for name in names:
-        if name == "qgz_bf16ef":
+        if name == "qgz_hier_ef":
+            w = wl.QGZ_HIERARCHICAL if args.scale == 1 else qgz_sample(wl.QGZ_HIERARCHICAL, args.scale)
+            line, _ = run_qgz(w, args, dev, dist, ws, hop1_ef=True)
+        elif name == "qgz_bf16ef":
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
             line, _ = run_qgz(w, args, dev, dist, ws, ef_bf16=True)
         elif name == "qgz_fused":

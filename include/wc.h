@@ -162,6 +162,23 @@ WC_API int wc_dequant_reduce_requant(const uint8_t *codes, const float *scales,
                                      void *stream);
 
 /*
+ * wc_dequant_reduce_requant_ef -- the first hop with error feedback on its
+ * requantization.  "Merge LoCo with Zero++" (review thread) keeps the error
+ * buffers on each parameter as `inter_ef_buf`, the buffer of the inter-node
+ * message; here every requantized value p keeps an fp32 error e1:
+ *   c = p + s * e1;  q, scale = Q4(c) per block;
+ *   e1 <- beta * e1 + (1 - beta) * (c - q * scale)   (1 - beta formed in fp32)
+ * ef1 : [R][G*S] fp32 in the layout of out_codes (unit u = g*L + l holds G*S
+ *       values), read and written in place, not NULL.  Start it at zero.
+ * Everything else as wc_dequant_reduce_requant.
+ */
+WC_API int wc_dequant_reduce_requant_ef(const uint8_t *codes, const float *scales,
+                                        int64_t N, int R, int G, int B,
+                                        uint8_t *out_codes, float *out_scales,
+                                        float *ef1, float err_scale,
+                                        float err_beta, void *stream);
+
+/*
  * wc_qgz_step_fused -- the whole flat step (G = 1) in one kernel: for every
  * destination block it runs wc_ef_quant_int4's arithmetic on the R ranks in
  * rank order and adds their dequantized values as wc_dequant_reduce does, so

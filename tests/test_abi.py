@@ -146,6 +146,10 @@ def test_bf16ef_and_replica_argument_errors(lib):
     assert f(FAKE, MIS, FAKE, FAKE, 1024, 4, 1, 256, 1.0, 0.5, None) == binding.WC_EALIGN
     assert f(FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 100, 1.0, 0.5, None) == binding.WC_EINVAL
     assert f(None, None, None, None, 0, 4, 1, 256, 1.0, 0.5, None) == binding.WC_OK
+    h = lib.wc_dequant_reduce_requant_ef
+    assert h(FAKE, FAKE, 8192, 8, 2, 256, FAKE, FAKE, None, 1.0, 0.5, None) == binding.WC_EINVAL
+    assert h(FAKE, FAKE, 8192, 8, 2, 256, FAKE, FAKE, MIS, 1.0, 0.5, None) == binding.WC_EALIGN
+    assert h(FAKE, FAKE, 8192, 8, 3, 256, FAKE, FAKE, FAKE, 1.0, 0.5, None) == binding.WC_EINVAL
     q = lib.wc_qwz_quant_replica_int8
     assert q(FAKE, FAKE, FAKE, None, 4096, 2048, None) == binding.WC_EINVAL
     assert q(FAKE, FAKE, FAKE, MIS, 4096, 2048, None) == binding.WC_EALIGN

@@ -71,6 +71,37 @@ def test_bf16_error_buffer_full_size(dev):
         assert_bits_equal(to_host(e_dev), e_cpu, f"bf16 error step {t}")
 
 
+HOP1_EF_CASES = [
+    # R, G, B, k (shard = k blocks), s, beta
+    (16, 2, 512, 3, 1.0, 0.5),      # the hierarchical workload's shape
+    (8, 2, 256, 4, 1.0, 0.0),
+    (8, 4, 128, 5, 2.0, 0.25),      # general kernel
+    (12, 3, 64, 7, 1.0, 0.5),       # general kernel, blocks shorter than the warp tile
+    (32, 2, 512, 1, 1.0, 0.5),      # 16 ranks per group
+    (16, 2, 1024, 1, 0.5, 0.75),
+]
+
+
+@pytest.mark.parametrize("R,G,B,k,s,beta", HOP1_EF_CASES)
+def test_first_hop_error_feedback_parity(dev, R, G, B, k, s, beta):
+    """Three chained steps; each side carries its own first-hop error."""
+    N = R * B * k
+    e1_cpu = np.zeros(G * N, np.float32)
+    e1_dev = torch.zeros(G * N, dtype=torch.float32, device=dev)
+    c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    for t in range(3):
+        g = edge_gradients(R, N, B, seed=101 * t + R + G)
+        cc, cs = ORC.ef_quant_int4(g, None, N, R, G, B, 1.0, 0.0)
+        binding.dequant_reduce_requant_ef(to_dev(cc, dev), to_dev(cs, dev), c1, s1, e1_dev, N, R,
+                                          G, B, s, beta)
+        torch.cuda.synchronize()
+        oc, os_ = ORC.dequant_reduce_requant_ef(cc, cs, N, R, G, B, e1_cpu, s, beta)
+        assert_bits_equal(to_host(c1), oc, f"hop-1 codes step {t}")
+        assert_bits_equal(to_host(s1), os_, f"hop-1 scales step {t}")
+        assert_bits_equal(to_host(e1_dev), e1_cpu, f"hop-1 error step {t}")
+
+
 @pytest.mark.parametrize("n,B", [(2048 * 21, 2048), (256 * 33, 256), (32 * 13, 32), (4096 * 2, 4096)])
 def test_qwz_replica_parity(dev, n, B):
     w = weights_with_edges(n, B, seed=3 * n + B)

@@ -149,6 +149,10 @@ HIER_CASES = [
     (8, 2, 32, 9),
     (8, 1, 256, 4),        # one group: first hop requantizes the flat reduce
     (4, 4, 1024, 1),       # one rank per group: first hop is a requantization
+    (32, 2, 512, 1),       # 16 ranks per group
+    (4, 2, 256, 3),        # 2 ranks per group
+    (16, 2, 1024, 1),      # 8 ranks per group, 1024-blocks
+    (6, 2, 512, 2),        # 3 ranks per group: general kernel at B = 512
 ]
 
 

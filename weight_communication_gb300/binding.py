@@ -29,6 +29,7 @@ SIGNATURES = {
     "wc_ef_quant_int4": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_dequant_reduce": [_P, _P, _I64, _I, _I, _I, _F, _P, _I, _P],
     "wc_dequant_reduce_requant": [_P, _P, _I64, _I, _I, _I, _P, _P, _P],
+    "wc_dequant_reduce_requant_ef": [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F, _P],
     "wc_qgz_step_fused": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
     "wc_ef_quant_int4_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
@@ -148,6 +149,20 @@ def dequant_reduce_requant(codes: torch.Tensor, scales: torch.Tensor, out_codes:
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B,
           _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
           _dev(out_scales, "out_scales", torch.float32, G * N // B, d), _stream(codes, stream))
+
+
+def dequant_reduce_requant_ef(codes: torch.Tensor, scales: torch.Tensor, out_codes: torch.Tensor,
+                              out_scales: torch.Tensor, ef1: torch.Tensor, N: int, R: int, G: int,
+                              B: int, err_scale: float = 1.0, err_beta: float = 0.0,
+                              stream=None) -> None:
+    """wc_dequant_reduce_requant_ef: first hop with error feedback on the
+    requantization; ef1 fp32 [G*N] updated in place."""
+    d = codes.device
+    _call("wc_dequant_reduce_requant_ef", _dev(codes, "codes", torch.uint8, R * N // 2, d),
+          _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B,
+          _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
+          _dev(out_scales, "out_scales", torch.float32, G * N // B, d),
+          _dev(ef1, "ef1", torch.float32, G * N, d), err_scale, err_beta, _stream(codes, stream))
 
 
 def qgz_step_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor | None,

@@ -137,7 +137,30 @@ WC_API int wc_dequant_reduce_requant(const uint8_t *codes, const float *scales, 
     WC_REQUIRE_PTR(fn, out_codes);
     WC_REQUIRE_PTR(fn, out_scales);
     return from_cuda(wc::launch_dequant_reduce_requant(codes, scales, out_codes, out_scales, geo,
-                                                       B, static_cast<cudaStream_t>(stream)),
+                                                       B, nullptr, 0.0f, 0.0f,
+                                                       static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_dequant_reduce_requant_ef(const uint8_t *codes, const float *scales, int64_t N,
+                                        int R, int G, int B, uint8_t *out_codes,
+                                        float *out_scales, float *ef1, float err_scale,
+                                        float err_beta, void *stream) {
+    static const char *fn = "wc_dequant_reduce_requant_ef";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (N * (int64_t)G >= (int64_t(1) << 32))
+        return fail(WC_ERANGE, "%s: G*N must be below 2^32", fn);
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    WC_REQUIRE_PTR(fn, out_codes);
+    WC_REQUIRE_PTR(fn, out_scales);
+    WC_REQUIRE_PTR(fn, ef1);
+    return from_cuda(wc::launch_dequant_reduce_requant(codes, scales, out_codes, out_scales, geo,
+                                                       B, ef1, err_scale, err_beta,
+                                                       static_cast<cudaStream_t>(stream)),
                      fn);
 }
 

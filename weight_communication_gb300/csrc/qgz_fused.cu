@@ -83,10 +83,11 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
             float *o = &eo.x;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float q = quant_code_f<7>(c[k][j], bs);
+                const QCode qc = quant_code<7>(c[k][j], bs);
+                const float q = qc.q;
                 const float d = dequant(q, bs.scale);
                 acc[k][j] = __fadd_rn(acc[k][j], d);
-                if (WRITE_CODES) packed |= (code_bits(q) & 15u) << (4 * j);
+                if (WRITE_CODES) packed |= (qc.bits & 15u) << (4 * j);
                 if (HAS_EF)
                     o[j] = __fadd_rn(__fmul_rn(beta, e[k][j]),
                                      __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));

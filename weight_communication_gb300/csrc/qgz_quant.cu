@@ -1,8 +1,8 @@
 // qgz_quant.cu -- kernels that produce int4 codes:
 //   * error-feedback compensation + int4 block quantization of every rank's
 //     gradient, written in all-to-all send order (LoCo on qgZ);
-//   * the first hop of the hierarchical reduce: dequantize the L chunks a
-//     unit receives from its group, add them in fp32, requantize to int4.
+//   (the first hop of the hierarchical reduce, which requantizes, is in
+//   qgz_hop1.cu).
 //
 // "Merge LoCo with Zero++" (DeepSpeed PR #6730), Overview: the 4-bit
 // gradients are compensated with an error-feedback buffer before they are
@@ -104,8 +104,9 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         uint32_t packed = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            q[j] = quant_code_f<7>(c[k][j], bs);
-            packed |= (code_bits(q[j]) & 15u) << (4 * j);
+            const QCode qc = quant_code<7>(c[k][j], bs);
+            q[j] = qc.q;
+            packed |= (qc.bits & 15u) << (4 * j);
         }
         const uint32_t in_blk = B >= 128 ? 128u * k + 4u * lane : (4u * lane) % B;
         const uint32_t pos = out0 + in_blk;
@@ -161,129 +162,6 @@ cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint
         case 256: return launch_ef_quant_b<256>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
         case 512: return launch_ef_quant_b<512>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
         case 1024: return launch_ef_quant_b<1024>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// First hop: dequantize L chunks, reduce in fp32, requantize to int4
-// ---------------------------------------------------------------------------
-//
-// Output element o (over all R units, G*S each) belongs to unit u = g*L + l,
-// sub-slice g' and offset i; its inputs are the codes at position
-// (g*L + l')*N + (l*G + g')*S + i for l' = 0..L-1.  Lane layout: warp tile
-// T = max(B, 256) outputs, lane t holds outputs 256*k + 8*t + j, i.e. one
-// 32-bit word of codes per source and per k: 128-byte coalesced loads and
-// stores per warp instruction.  The exact fp32 chain (one multiply and one
-// add per code, in source order) makes this kernel issue-bound rather than
-// HBM-bound at L = 8 (about 4.4 fp32/int operations per code read).
-template <int B>
-__global__ void __launch_bounds__(256)
-dequant_reduce_requant_kernel(const uint8_t *__restrict__ codes,
-                              const float *__restrict__ scales,
-                              uint8_t *__restrict__ out_codes,
-                              float *__restrict__ out_scales, QgzGeometry geo) {
-    constexpr int T = B >= 256 ? B : 256;
-    constexpr int K = T / 256;
-    constexpr int LPB = B >= 256 ? 32 : B / 8;
-    const int lane = threadIdx.x & (kWarp - 1);
-    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
-    const uint32_t total_out = geo.G * geo.N;  // R units * G*S
-    if (uint64_t(warp) * T >= total_out) return;
-    const uint32_t tile0 = warp * uint32_t(T);
-
-    const uint32_t unit_len = geo.G * geo.S;
-    const uint32_t cstride = geo.N / 2;  // bytes between consecutive ranks' codes
-    const uint32_t sstride = geo.N / B;  // scales between consecutive ranks
-    float acc[K][8];
-    bool active[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const uint32_t o = tile0 + 256u * k + 8u * lane;
-        active[k] = o < total_out;
-        const uint32_t oo = active[k] ? o : tile0;
-        const uint32_t u = oo / unit_len;
-        const uint32_t rem = oo - u * unit_len;
-        const uint32_t gq = rem / geo.S;
-        const uint32_t i = rem - gq * geo.S;
-        const uint32_t grp = u / geo.L;
-        const uint32_t l = u - grp * geo.L;
-        const uint32_t pos0 = grp * geo.L * geo.N + (l * geo.G + gq) * geo.S + i;
-        const uint8_t *cp = codes + pos0 / 2;
-        const float *sp = scales + pos0 / B;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[k][j] = 0.0f;
-        if (!active[k]) continue;
-        // Loads for up to 8 sources first, then the adds in source order.
-        for (uint32_t l0 = 0; l0 < geo.L; l0 += 8) {
-            uint32_t w[8];
-            float sc[8];
-            const uint32_t nb = min(8u, geo.L - l0);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (t < nb) {
-                    w[t] = __ldcs(reinterpret_cast<const unsigned int *>(cp + (l0 + t) * cstride));
-                    sc[t] = __ldg(sp + (l0 + t) * sstride);
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (t < nb) {
-                    float f[8];
-                    unpack_int4x8(w[t], f);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        acc[k][j] = __fadd_rn(acc[k][j], dequant(f[j], sc[t]));
-                }
-            }
-        }
-    }
-
-    float m = 0.0f;
-#pragma unroll
-    for (int k = 0; k < K; ++k)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(acc[k][j]));
-    m = group_max<LPB>(m);
-    const BlockScale bs = block_scale<7>(m);
-
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        if (!active[k]) continue;
-        const uint32_t o = tile0 + 256u * k + 8u * lane;
-        uint32_t packed = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            packed |= (code_bits(quant_code_f<7>(acc[k][j], bs)) & 15u) << (4 * j);
-        __stcs(reinterpret_cast<unsigned int *>(out_codes + o / 2), packed);
-        if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
-    }
-}
-
-template <int B>
-static cudaError_t launch_drq_b(const uint8_t *codes, const float *scales, uint8_t *out_codes,
-                                float *out_scales, const QgzGeometry &geo,
-                                cudaStream_t stream) {
-    constexpr int T = B >= 256 ? B : 256;
-    const uint32_t total_out = geo.G * geo.N;
-    const uint32_t tiles = (total_out + T - 1) / T;
-    const uint32_t threads = 256;
-    const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
-    dequant_reduce_requant_kernel<B><<<grid, threads, 0, stream>>>(codes, scales, out_codes,
-                                                                    out_scales, geo);
-    return cudaPeekAtLastError();
-}
-
-cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *scales,
-                                          uint8_t *out_codes, float *out_scales,
-                                          const QgzGeometry &geo, int B, cudaStream_t stream) {
-    switch (B) {
-        case 32: return launch_drq_b<32>(codes, scales, out_codes, out_scales, geo, stream);
-        case 64: return launch_drq_b<64>(codes, scales, out_codes, out_scales, geo, stream);
-        case 128: return launch_drq_b<128>(codes, scales, out_codes, out_scales, geo, stream);
-        case 256: return launch_drq_b<256>(codes, scales, out_codes, out_scales, geo, stream);
-        case 512: return launch_drq_b<512>(codes, scales, out_codes, out_scales, geo, stream);
-        case 1024: return launch_drq_b<1024>(codes, scales, out_codes, out_scales, geo, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -13,97 +13,175 @@
 // the first-hop outputs of its L units, N elements in all), c(k) = l*G + g
 // for k = g*L + l.
 //
-// Grid: y = destination, x = 8-output groups of its shard.  One thread makes
-// 8 consecutive outputs: per source one 32-bit word of codes (coalesced,
-// 128 B per warp instruction) and one scale, then the 8 sums in source
-// order.  Sources are fetched 8 at a time before any add, so that enough
-// loads are in flight per thread; the codes are unpacked with byte permutes
-// and exact fp32 subtractions (wc_device.cuh), keeping the conversion pipe
-// idle -- the per-code work is one permute, one subtract, one multiply and
-// one add.
+// The per-code work -- unpack, multiply by the scale, add in source order --
+// is all the kernel does besides moving bytes, so it runs issue-bound unless
+// the instruction count per code stays near its floor of one byte permute
+// and three exact fp32 operations.  Hence: the source count is a template
+// parameter (no loop bounds, no guards, every load hoisted ahead of the
+// adds), each thread makes 16 consecutive outputs from one 8-byte code word
+// per source (so the per-source address and scale work is amortized over 16
+// codes), the destination comes from the grid's y index (no division), and
+// codes are unpacked with byte permutes and exact subtractions
+// (wc_device.cuh), never on the conversion pipe.  Source counts above
+// kMaxFixedSources take a loop over batches of eight.
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
 namespace wc {
 
+constexpr int kMaxFixedSources = 16;
+constexpr uint32_t kOutPerThread = 16;
+
 template <bool OUT_BF16>
-__global__ void __launch_bounds__(256)
-dequant_reduce_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
-                      QgzGeometry geo, uint32_t nsrc, uint32_t log2_b, float out_scale,
-                      void *__restrict__ out) {
-    const uint32_t k = blockIdx.y;  // destination
-    const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (uint64_t(v) * 8u >= geo.S) return;
-    const uint32_t i = v * 8u;  // offset in the shard
+__device__ __forceinline__ void store16(void *out, uint32_t o, const float acc[16], float out_scale) {
+    if (OUT_BF16) {
+        uint32_t h[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = f32_to_bf16_bits(__fmul_rn(acc[j], out_scale));
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
+        __stcs(dst, make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                               h[6] | (h[7] << 16)));
+        __stcs(dst + 1, make_uint4(h[8] | (h[9] << 16), h[10] | (h[11] << 16),
+                                   h[12] | (h[13] << 16), h[14] | (h[15] << 16)));
+    } else {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            __stcs(dst + q, make_float4(__fmul_rn(acc[4 * q], out_scale),
+                                        __fmul_rn(acc[4 * q + 1], out_scale),
+                                        __fmul_rn(acc[4 * q + 2], out_scale),
+                                        __fmul_rn(acc[4 * q + 3], out_scale)));
+    }
+}
+
+// acc[0..16) += the 16 codes of w (element 2k in the low nibble of byte k) * sc
+__device__ __forceinline__ void accumulate16(uint2 w, float sc, float acc[16]) {
+    float f[8];
+    unpack_int4x8(w.x, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], dequant(f[j], sc));
+    unpack_int4x8(w.y, f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[8 + j] = __fadd_rn(acc[8 + j], dequant(f[j], sc));
+}
+
+// First code position and scale index of destination k's 16 outputs at i.
+__device__ __forceinline__ uint32_t source_base(const QgzGeometry &geo, uint32_t k, uint32_t i) {
     uint32_t chunk = k;
     if (geo.G > 1) {
         const uint32_t grp = k / geo.L;
         chunk = (k - grp * geo.L) * geo.G + grp;
     }
-    const uint32_t base = chunk * geo.S + i;
+    return chunk * geo.S + i;
+}
+
+template <int NSRC, bool OUT_BF16>
+__global__ void __launch_bounds__(256)
+dequant_reduce_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
+                            QgzGeometry geo, uint32_t log2_b, float out_scale,
+                            void *__restrict__ out) {
+    const uint32_t k = blockIdx.y;  // destination
+    const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (uint64_t(v) * kOutPerThread >= geo.S) return;
+    const uint32_t i = v * kOutPerThread;  // offset in the shard
+    const uint32_t base = source_base(geo, k, i);
     const uint8_t *cp = codes + base / 2;
     const float *sp = scales + (base >> log2_b);
-    const uint32_t cstride = geo.N / 2;         // bytes between sources
-    const uint32_t sstride = geo.N >> log2_b;   // scales between sources
+    const uint32_t cstride = geo.N / 2;        // bytes between sources
+    const uint32_t sstride = geo.N >> log2_b;  // scales between sources
 
-    float acc[8];
+    uint2 w[NSRC];
+    float sc[NSRC];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (uint32_t s0 = 0; s0 < nsrc; s0 += 8) {
-        uint32_t w[8];
+    for (int t = 0; t < NSRC; ++t) {
+        w[t] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride));
+        sc[t] = __ldg(sp + size_t(t) * sstride);
+    }
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+#pragma unroll
+    for (int t = 0; t < NSRC; ++t) accumulate16(w[t], sc[t], acc);
+    store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
+}
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256)
+dequant_reduce_loop_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
+                           QgzGeometry geo, uint32_t nsrc, uint32_t log2_b, float out_scale,
+                           void *__restrict__ out) {
+    const uint32_t k = blockIdx.y;
+    const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (uint64_t(v) * kOutPerThread >= geo.S) return;
+    const uint32_t i = v * kOutPerThread;
+    const uint32_t base = source_base(geo, k, i);
+    const uint8_t *cp = codes + base / 2;
+    const float *sp = scales + (base >> log2_b);
+    const uint32_t cstride = geo.N / 2;
+    const uint32_t sstride = geo.N >> log2_b;
+
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+    uint32_t t = 0;
+    for (; t + 8 <= nsrc; t += 8) {
+        uint2 w[8];
         float sc[8];
-        const uint32_t nb = min(8u, nsrc - s0);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (t < nb) {
-                w[t] = __ldcs(reinterpret_cast<const unsigned int *>(cp + (s0 + t) * cstride));
-                sc[t] = __ldg(sp + (s0 + t) * sstride);
-            }
+        for (int u = 0; u < 8; ++u) {
+            w[u] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t + u) * cstride));
+            sc[u] = __ldg(sp + size_t(t + u) * sstride);
         }
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (t < nb) {
-                float f[8];
-                unpack_int4x8(w[t], f);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], dequant(f[j], sc[t]));
-            }
-        }
+        for (int u = 0; u < 8; ++u) accumulate16(w[u], sc[u], acc);
     }
+    for (; t < nsrc; ++t)
+        accumulate16(__ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride)),
+                     __ldg(sp + size_t(t) * sstride), acc);
+    store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
+}
 
-    const uint32_t o = k * geo.S + i;
-    if (OUT_BF16) {
-        uint32_t h[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) h[j] = f32_to_bf16_bits(__fmul_rn(acc[j], out_scale));
-        uint4 pk = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                              h[6] | (h[7] << 16));
-        __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o), pk);
-    } else {
-        float *dst = static_cast<float *>(out) + o;
-        __stcs(reinterpret_cast<float4 *>(dst),
-               make_float4(__fmul_rn(acc[0], out_scale), __fmul_rn(acc[1], out_scale),
-                           __fmul_rn(acc[2], out_scale), __fmul_rn(acc[3], out_scale)));
-        __stcs(reinterpret_cast<float4 *>(dst + 4),
-               make_float4(__fmul_rn(acc[4], out_scale), __fmul_rn(acc[5], out_scale),
-                           __fmul_rn(acc[6], out_scale), __fmul_rn(acc[7], out_scale)));
+template <int NSRC, bool OUT_BF16>
+static void launch_fixed(const uint8_t *codes, const float *scales, const QgzGeometry &geo,
+                         uint32_t log2_b, float out_scale, void *out, dim3 grid,
+                         cudaStream_t stream) {
+    dequant_reduce_fixed_kernel<NSRC, OUT_BF16><<<grid, 256, 0, stream>>>(codes, scales, geo,
+                                                                          log2_b, out_scale, out);
+}
+
+template <bool OUT_BF16>
+static void launch_any(const uint8_t *codes, const float *scales, const QgzGeometry &geo,
+                       uint32_t nsrc, uint32_t log2_b, float out_scale, void *out, dim3 grid,
+                       cudaStream_t stream) {
+#define WC_FIXED(n)                                                                         \
+    case n:                                                                                 \
+        launch_fixed<n, OUT_BF16>(codes, scales, geo, log2_b, out_scale, out, grid, stream); \
+        return;
+    switch (nsrc) {
+        WC_FIXED(1) WC_FIXED(2) WC_FIXED(3) WC_FIXED(4) WC_FIXED(5) WC_FIXED(6) WC_FIXED(7)
+        WC_FIXED(8) WC_FIXED(9) WC_FIXED(10) WC_FIXED(11) WC_FIXED(12) WC_FIXED(13)
+        WC_FIXED(14) WC_FIXED(15) WC_FIXED(16)
+        default:
+            dequant_reduce_loop_kernel<OUT_BF16><<<grid, 256, 0, stream>>>(
+                codes, scales, geo, nsrc, log2_b, out_scale, out);
     }
+#undef WC_FIXED
 }
 
 cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
                                   const QgzGeometry &geo, int B, float out_scale, void *out,
                                   bool out_bf16, cudaStream_t stream) {
+    static_assert(kMaxFixedSources == 16, "dispatch table covers 1..16");
     uint32_t log2_b = 0;
     while ((1u << log2_b) < uint32_t(B)) ++log2_b;
     const uint32_t nsrc = geo.G > 1 ? geo.G : geo.R;
     const uint32_t threads = 256;
-    const dim3 grid((geo.S / 8 + threads - 1) / threads, geo.R);
+    // S is a multiple of B >= 32, hence of the 16 outputs a thread makes
+    const dim3 grid((geo.S / kOutPerThread + threads - 1) / threads, geo.R);
     if (out_bf16)
-        dequant_reduce_kernel<true><<<grid, threads, 0, stream>>>(codes, scales, geo, nsrc,
-                                                                   log2_b, out_scale, out);
+        launch_any<true>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
     else
-        dequant_reduce_kernel<false><<<grid, threads, 0, stream>>>(codes, scales, geo, nsrc,
-                                                                    log2_b, out_scale, out);
+        launch_any<false>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
     return cudaPeekAtLastError();
 }
 

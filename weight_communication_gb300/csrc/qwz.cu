@@ -58,8 +58,9 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t half = (j & 1) ? (h[j / 2] >> 16) : (h[j / 2] & 0xFFFFu);
-            const float q = quant_code_f<127>(bf16_bits_to_f32(half), bs);
-            word[j / 4] |= (code_bits(q) & 0xFFu) << (8 * (j % 4));
+            const QCode qc = quant_code<127>(bf16_bits_to_f32(half), bs);
+            const float q = qc.q;
+            word[j / 4] |= (qc.bits & 0xFFu) << (8 * (j % 4));
             if (REPLICA)
                 rep[j / 2] |= uint32_t(f32_to_bf16_bits(dequant(q, bs.scale))) << (16 * (j & 1));
         }

@@ -66,22 +66,25 @@ __device__ __forceinline__ BlockScale block_scale(float m) {
 // two's complement, because the constant's low 22 bits are zero.
 constexpr float kRoundShift = 12582912.0f;  // 1.5 * 2^23
 
-__device__ __forceinline__ float round_half_even_small(float x) {
-    return __fsub_rn(__fadd_rn(x, kRoundShift), kRoundShift);
-}
+// Code of one value of a block: q = clamp(rint(x * inv), -QMAX, QMAX), as an
+// exact integer-valued float together with its two's-complement bits (the
+// caller masks the low 4 or 8), both from the one rounding addition.
+// No clamp is executed because none can be active: every |x| of the block
+// is at most m, inv = fl(QMAX / m) <= (QMAX / m)(1 + 2^-24), so
+// |x * inv| <= QMAX (1 + 2^-24)^2 < QMAX + 1/2 after its own rounding, and
+// rint returns at most QMAX; a zero block has inv = 0 and gives q = 0.
+struct QCode {
+    float q;
+    uint32_t bits;
+};
 
-// Code of one value, as an exact integer-valued float:
-// clamp(rint(x * inv), -QMAX, QMAX).  (|x * inv| <= QMAX * (1 + 2^-23) for
-// every value of the block, so the clamp only guards the definition.)
 template <int QMAX>
-__device__ __forceinline__ float quant_code_f(float x, const BlockScale &s) {
-    const float q = round_half_even_small(__fmul_rn(x, s.inv));
-    return fminf(fmaxf(q, -float(QMAX)), float(QMAX));
-}
-
-// Two's-complement bits of an integer-valued float q, |q| < 2^22 (caller masks).
-__device__ __forceinline__ uint32_t code_bits(float q) {
-    return __float_as_uint(__fadd_rn(q, kRoundShift));
+__device__ __forceinline__ QCode quant_code(float x, const BlockScale &s) {
+    const float r = __fadd_rn(__fmul_rn(x, s.inv), kRoundShift);
+    QCode c;
+    c.bits = __float_as_uint(r);
+    c.q = __fsub_rn(r, kRoundShift);
+    return c;
 }
 
 // Dequantized value: code * scale, one rounding.

@@ -26,9 +26,11 @@ cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint
 cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
                                   const QgzGeometry &geo, int B, float out_scale, void *out,
                                   bool out_bf16, cudaStream_t stream);
+// ef1: fp32 [G*N] error of every requantized value (unit order), or NULL.
 cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *scales,
                                           uint8_t *out_codes, float *out_scales,
-                                          const QgzGeometry &geo, int B, cudaStream_t stream);
+                                          const QgzGeometry &geo, int B, float *ef1, float s,
+                                          float beta, cudaStream_t stream);
 cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
                                   const QgzGeometry &geo, int B, float s, float beta,
                                   float out_scale, void *out, bool out_bf16,

@@ -30,9 +30,12 @@ class QgzReducer:
 
     def __init__(self, N: int, R: int, G: int = 1, B: int = 256, err_scale: float = 1.0,
                  err_beta: float = 0.0, use_ef: bool = True, out_dtype=torch.float32,
-                 out_scale: float = 1.0, device="cuda", ef_dtype=torch.float32):
+                 out_scale: float = 1.0, device="cuda", ef_dtype=torch.float32,
+                 hop1_ef: bool = False):
         """ef_dtype: torch.float32, or torch.bfloat16 for the half-size error
-        buffer (wc_ef_quant_int4_bf16ef)."""
+        buffer (wc_ef_quant_int4_bf16ef).  hop1_ef (G > 1): keep an fp32 error
+        for the first hop's requantization too (wc_dequant_reduce_requant_ef),
+        with the same err_scale and err_beta."""
         self.N, self.R, self.G, self.B = N, R, G, B
         self.err_scale, self.err_beta = err_scale, err_beta
         self.out_scale = out_scale
@@ -48,6 +51,7 @@ class QgzReducer:
             self.scales1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
         else:
             self.codes1 = self.scales1 = None
+        self.ef1 = torch.zeros(G * N, dtype=torch.float32, device=dev) if (hop1_ef and G > 1) else None
         self.out = torch.empty(N, dtype=out_dtype, device=dev)
 
     @property
@@ -63,16 +67,30 @@ class QgzReducer:
             binding.ef_quant_int4(g.reshape(-1), self.ef, self.codes, self.scales, self.N, self.R,
                                   self.G, self.B, self.err_scale, self.err_beta, stream)
 
-    def reduce(self, stream=None) -> torch.Tensor:
-        if self.G > 1:
+    def reduce_first_hop(self, stream=None) -> None:
+        """G > 1: the intra-group dequant-reduce-requant into codes1/scales1."""
+        if self.ef1 is not None:
+            binding.dequant_reduce_requant_ef(self.codes, self.scales, self.codes1, self.scales1,
+                                              self.ef1, self.N, self.R, self.G, self.B,
+                                              self.err_scale, self.err_beta, stream)
+        else:
             binding.dequant_reduce_requant(self.codes, self.scales, self.codes1, self.scales1,
                                            self.N, self.R, self.G, self.B, stream)
+
+    def reduce_last_hop(self, stream=None) -> torch.Tensor:
+        """The dequant-reduce into the shards: flat, or the inter-group hop."""
+        if self.G > 1:
             binding.dequant_reduce(self.codes1, self.scales1, self.out, self.N, self.R, self.G,
                                    self.B, self.out_scale, stream)
         else:
             binding.dequant_reduce(self.codes, self.scales, self.out, self.N, self.R, 1, self.B,
                                    self.out_scale, stream)
         return self.out
+
+    def reduce(self, stream=None) -> torch.Tensor:
+        if self.G > 1:
+            self.reduce_first_hop(stream)
+        return self.reduce_last_hop(stream)
 
     def step(self, g: torch.Tensor, stream=None) -> torch.Tensor:
         """Quantize every rank's gradient g ([R, N] bf16 on the device) and
