@@ -114,3 +114,50 @@ def test_qwz_replica_parity(dev, n, B):
     assert_bits_equal(to_host(codes), oc, "codes")
     assert_bits_equal(to_host(scales), os_, "scales")
     assert_bits_equal(to_host(rep), orep, "replica")
+
+
+def test_host_pipeline_matches_serial_steps(dev):
+    """Pipelined host-to-host steps give the same shards and error buffer as
+    the same steps run one after another on one stream."""
+    from weight_communication_gb300.qgz import HostPipeline, QgzReducer
+    for w in (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 64), wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 8)):
+        out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+        a = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                       hop1_ef=w.G > 1)
+        b = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                       hop1_ef=w.G > 1)
+        steps = 5
+        g_host = [wl.qgz_gradients(w, t).pin_memory() for t in range(steps)]
+        out_host = [torch.empty(w.N, dtype=out_dtype).pin_memory() for _ in range(steps)]
+        HostPipeline(a).run(g_host, out_host)
+        torch.cuda.synchronize()
+        for t in range(steps):
+            want = b.step(g_host[t].to(dev).view(-1)).cpu()
+            assert torch.equal(out_host[t].view(torch.int16) if out_dtype == torch.bfloat16
+                               else out_host[t].view(torch.int32),
+                               want.view(torch.int16) if out_dtype == torch.bfloat16
+                               else want.view(torch.int32)), (w.name, t)
+        assert torch.equal(a.ef.view(torch.int32), b.ef.view(torch.int32))
+        if w.G > 1:
+            assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32))
+
+
+def test_reducer_with_first_hop_error_feedback_matches_oracle(dev):
+    """QgzReducer's hierarchical step with error feedback on both hops,
+    two chained steps, against the oracle's composition."""
+    from weight_communication_gb300.qgz import QgzReducer
+    w = wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 6)
+    red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=torch.bfloat16,
+                     device=dev, hop1_ef=True)
+    e = np.zeros(w.R * w.N, np.float32)
+    e1 = np.zeros(w.G * w.N, np.float32)
+    for t in range(2):
+        g = wl.qgz_gradients(w, t, device=dev)
+        out = red.step(g)
+        torch.cuda.synchronize()
+        gu = to_host(g).ravel()
+        cc, cs = ORC.ef_quant_int4(gu, e, w.N, w.R, w.G, w.B, w.err_scale, w.err_beta)
+        c1, s1 = ORC.dequant_reduce_requant_ef(cc, cs, w.N, w.R, w.G, w.B, e1, w.err_scale, w.err_beta)
+        want = ORC.dequant_reduce(c1, s1, w.N, w.R, w.G, w.B, 1.0, True)
+        assert_bits_equal(to_host(out), want, f"shards step {t}")
+        assert_bits_equal(to_host(red.ef1), e1, f"first-hop error step {t}")

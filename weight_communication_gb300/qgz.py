@@ -77,15 +77,17 @@ class QgzReducer:
             binding.dequant_reduce_requant(self.codes, self.scales, self.codes1, self.scales1,
                                            self.N, self.R, self.G, self.B, stream)
 
-    def reduce_last_hop(self, stream=None) -> torch.Tensor:
-        """The dequant-reduce into the shards: flat, or the inter-group hop."""
+    def reduce_last_hop(self, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+        """The dequant-reduce into the shards (self.out unless `out` is
+        given): flat, or the inter-group hop."""
+        out = self.out if out is None else out
         if self.G > 1:
-            binding.dequant_reduce(self.codes1, self.scales1, self.out, self.N, self.R, self.G,
+            binding.dequant_reduce(self.codes1, self.scales1, out, self.N, self.R, self.G,
                                    self.B, self.out_scale, stream)
         else:
-            binding.dequant_reduce(self.codes, self.scales, self.out, self.N, self.R, 1, self.B,
+            binding.dequant_reduce(self.codes, self.scales, out, self.N, self.R, 1, self.B,
                                    self.out_scale, stream)
-        return self.out
+        return out
 
     def reduce(self, stream=None) -> torch.Tensor:
         if self.G > 1:
@@ -109,3 +111,58 @@ class QgzReducer:
             self.step(g_dev, s)
             out_host.copy_(self.out, non_blocking=True)
         return out_host
+
+
+class HostPipeline:
+    """Steps of a QgzReducer from pinned host gradients to pinned host shards,
+    with each step's host->device copy, kernels and device->host copy
+    overlapped with its neighbours' on three streams (the two copy
+    directions use separate copy engines; the kernels keep their order on
+    one stream, so the error buffer sees the steps in sequence).
+
+    Two device buffers of each kind rotate: step i's gradient goes to
+    g_dev[i % 2] once step i-2's quantization has read it, and its shards
+    come from out_dev[i % 2] once step i-2's copy to the host has finished.
+    """
+
+    def __init__(self, red: QgzReducer):
+        self.red = red
+        dev = red.device
+        self.g_dev = [torch.empty(red.R * red.N, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.out_dev = [torch.empty_like(red.out) for _ in range(2)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.comp = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.g_loaded = [torch.cuda.Event() for _ in range(2)]
+        self.g_consumed = [torch.cuda.Event() for _ in range(2)]
+        self.out_ready = [torch.cuda.Event() for _ in range(2)]
+        self.out_copied = [torch.cuda.Event() for _ in range(2)]
+        self._started = [False, False]
+
+    def run(self, g_host: list, out_host: list) -> None:
+        """Step i reads g_host[i] (pinned, R*N bf16) and writes out_host[i]
+        (pinned, like red.out).  Asynchronous: the caller synchronizes (or
+        waits on self.d2h) before reading out_host."""
+        red = self.red
+        for i, (gh, oh) in enumerate(zip(g_host, out_host)):
+            b = i % 2
+            with torch.cuda.stream(self.h2d):
+                if self._started[b]:
+                    self.h2d.wait_event(self.g_consumed[b])
+                self.g_dev[b].copy_(gh.view(-1), non_blocking=True)
+                self.g_loaded[b].record(self.h2d)
+            with torch.cuda.stream(self.comp):
+                self.comp.wait_event(self.g_loaded[b])
+                red.quantize(self.g_dev[b], self.comp)
+                self.g_consumed[b].record(self.comp)
+                if self._started[b]:
+                    self.comp.wait_event(self.out_copied[b])
+                if red.G > 1:
+                    red.reduce_first_hop(self.comp)
+                red.reduce_last_hop(self.comp, out=self.out_dev[b])
+                self.out_ready[b].record(self.comp)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(self.out_ready[b])
+                oh.copy_(self.out_dev[b], non_blocking=True)
+                self.out_copied[b].record(self.d2h)
+            self._started[b] = True
