@@ -284,42 +284,94 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         if timer is not None:
             timer.mark(ti, len(names))
 
+    # With an L2-resident workload the steps are timed one by one with an L2
+    # flush between them; otherwise steps run back to back, the reduce of
+    # each on a second stream beside the next quantization (DevicePipeline),
+    # unless --no-overlap.
+    overlap = flush is None and not args.no_overlap
+    sampler = None
+
+    def serial_pass(n_steps, with_clocks):
+        nonlocal sampler
+        timer = Timer(names, n_steps)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda.synchronize(dev)
+            if with_clocks and args.clocks:
+                sampler = ClockSampler(dev.index or 0)
+                time.sleep(0.2)
+            barrier(dist)
+            torch.cuda.synchronize(dev)
+            t0 = time.time()
+            start.record()
+            for i in range(n_steps):
+                step(args.warmup + i, timer, i)
+                if flush is not None:
+                    flush_l2(flush)
+            end.record()
+            torch.cuda.synchronize(dev)
+            t1 = time.time()
+            barrier(dist)
+        return timer, start.elapsed_time(end) / n_steps, (t0, t1)
+
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
             if flush is not None:
                 flush_l2(flush)
+    serial_steps = args.steps if not overlap else max(1, min(args.steps, 200))
+    timer, serial_ms, (t0, t1) = serial_pass(serial_steps, with_clocks=not overlap)
+    per_kernel = timer.per_kernel_ms()
+    overlapped = None
+    if overlap:
+        from weight_communication_gb300.qgz import DevicePipeline
+        pipe = DevicePipeline(red)
+        spans = {"quant": [[None, None] for _ in range(args.steps)],
+                 "reduce": [[None, None] for _ in range(args.steps)]}
+        for i in range(args.warmup):
+            pipe.step(batches[i % nbatch])
         torch.cuda.synchronize(dev)
-        timer = Timer(names, args.steps)
+
+        def mark(kind, i, which, st):
+            if i >= pipe_base:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(st)
+                spans[kind][i - pipe_base][0 if which == "begin" else 1] = ev
+
+        pipe_base = pipe.count
+        pipe.timer = mark
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        sampler = ClockSampler(dev.index or 0) if args.clocks else None
-        time.sleep(0.2 if sampler else 0)
+        if args.clocks:
+            sampler = ClockSampler(dev.index or 0)
+            time.sleep(0.2)
         barrier(dist)
         torch.cuda.synchronize(dev)
         t0 = time.time()
-        start.record()
+        start.record(pipe.quant_stream)
         for i in range(args.steps):
-            step(args.warmup + i, timer, i)
-            if flush is not None:
-                flush_l2(flush)
-        end.record()
+            pipe.step(batches[(args.warmup + i) % nbatch])
+        end.record(pipe.reduce_stream)
         torch.cuda.synchronize(dev)
         t1 = time.time()
         barrier(dist)
-        clocks = sampler.stop(t0, t1) if sampler else None
-    per_kernel = timer.per_kernel_ms()
-    # With an L2 flush between steps the flush is not part of the step: the
-    # step time is the kernels' event span; otherwise it is the whole region.
-    ms_local = timer.step_sum_ms() if flush is not None else start.elapsed_time(end) / args.steps
+        overlapped = {k: statistics.mean(b.elapsed_time(e) for b, e in v) for k, v in spans.items()}
+        ms_local = start.elapsed_time(end) / args.steps
+    elif flush is not None:
+        # the flush is not part of the step: the step time is the kernels' span
+        ms_local = timer.step_sum_ms()
+    else:
+        ms_local = serial_ms
+    clocks = sampler.stop(t0, t1) if sampler else None
     ms = max_over_ranks(ms_local, dist, dev)
     units = w.R * w.N
     value = job_throughput(units, ws, ms)
 
-    # roofline of the dominant kernel (the error-feedback quantization)
+    # roofline of the dominant kernel (the error-feedback quantization), from
+    # its launches inside the timed region
     peak, peak_kind = measured_peaks()
     ef_bytes = 2 if ef_bf16 else 4
     efq_bytes = w.R * w.N * (2 + 2 * ef_bytes + 0.5) + w.R * w.N // w.B * 4
-    efq_ms = per_kernel["ef_quant_int4"]
+    efq_ms = overlapped["quant"] if overlapped else per_kernel["ef_quant_int4"]
     achieved = efq_bytes / (efq_ms / 1e3) / 1e9
     efq_kernel = "ef_quant_int4_bf16ef" if ef_bf16 else "ef_quant_int4"
     traffic = ncu_traffic(efq_kernel, w.name.split()[0], units) if not ef_bf16 else None
@@ -350,6 +402,9 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
                    "out": "bf16" if w.out_bf16 else "fp32",
                    "l2": ("flushed between steps (untimed 516 MB write)" if flush is not None
                           else f"inputs exceed L2 ({units * 10 / 1e9:.1f} GB per step)"),
+                   "steps_overlap": ("each step's reduce runs on a second stream beside the "
+                                     "next step's EF-quant (event-ordered)" if overlap
+                                     else "none: steps one after another on one stream"),
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "kernel": efq_kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
@@ -359,6 +414,11 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         "gpu_launches": args.steps * len(names),
         "clocks": clocks,
     }
+    if overlapped:
+        line["overlapped_spans_ms"] = {"ef_quant_int4": round(overlapped["quant"], 5),
+                                       "reduce": round(overlapped["reduce"], 5)}
+        line["serial_ms_per_step"] = max_over_ranks(serial_ms, dist, dev)
+        line["kernels_from"] = f"serial pass of {serial_steps} steps (one stream)"
     if not args.no_e2e:
         line["e2e"] = run_qgz_e2e(w, red, batches[0], args, dev, dist, ws, stream)
     return line, batches[0]
@@ -667,6 +727,8 @@ def main(argv=None):
                              "qgz_hierarchical", "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="time qgZ steps one after another on one stream")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--scale", type=int, default=1,
                     help="divide each rank's gradient by this (profiling a smaller case)")

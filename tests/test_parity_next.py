@@ -161,3 +161,33 @@ def test_reducer_with_first_hop_error_feedback_matches_oracle(dev):
         want = ORC.dequant_reduce(c1, s1, w.N, w.R, w.G, w.B, 1.0, True)
         assert_bits_equal(to_host(out), want, f"shards step {t}")
         assert_bits_equal(to_host(red.ef1), e1, f"first-hop error step {t}")
+
+
+def test_device_pipeline_matches_serial_steps(dev):
+    """Steps with the reduce on a second stream give the same shards, error
+    buffers and (hierarchical) first-hop errors as serial steps."""
+    from weight_communication_gb300.qgz import DevicePipeline, QgzReducer
+    for w in (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 64), wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 8)):
+        out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+        a = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                       hop1_ef=w.G > 1)
+        b = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                       hop1_ef=w.G > 1)
+        pipe = DevicePipeline(a)
+        grads = [wl.qgz_gradients(w, t, device=dev) for t in range(5)]
+        outs = []
+        for t in range(5):
+            pipe.step(grads[t])
+            snap = torch.empty_like(a.out)
+            pipe.reduce_stream.wait_stream(pipe.reduce_stream)
+            with torch.cuda.stream(pipe.reduce_stream):
+                snap.copy_(a.out)
+            outs.append(snap)
+        torch.cuda.synchronize()
+        for t in range(5):
+            want = b.step(grads[t])
+            assert torch.equal(outs[t].view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32),
+                               want.view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32)), t
+        assert torch.equal(a.ef.view(torch.int32), b.ef.view(torch.int32))
+        if w.G > 1:
+            assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32))

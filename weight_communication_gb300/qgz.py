@@ -58,26 +58,31 @@ class QgzReducer:
     def launches_per_step(self) -> int:
         return 3 if self.G > 1 else 2
 
-    def quantize(self, g: torch.Tensor, stream=None) -> None:
+    def quantize(self, g: torch.Tensor, stream=None, send=None) -> None:
+        """EF-quant of every rank into the send buffers (self.codes,
+        self.scales, or the (codes, scales) pair `send`)."""
+        codes, scales = send if send is not None else (self.codes, self.scales)
         if self.ef is not None and self.ef.dtype == torch.bfloat16:
-            binding.ef_quant_int4_bf16ef(g.reshape(-1), self.ef, self.codes, self.scales, self.N,
+            binding.ef_quant_int4_bf16ef(g.reshape(-1), self.ef, codes, scales, self.N,
                                          self.R, self.G, self.B, self.err_scale, self.err_beta,
                                          stream)
         else:
-            binding.ef_quant_int4(g.reshape(-1), self.ef, self.codes, self.scales, self.N, self.R,
+            binding.ef_quant_int4(g.reshape(-1), self.ef, codes, scales, self.N, self.R,
                                   self.G, self.B, self.err_scale, self.err_beta, stream)
 
-    def reduce_first_hop(self, stream=None) -> None:
+    def reduce_first_hop(self, stream=None, send=None) -> None:
         """G > 1: the intra-group dequant-reduce-requant into codes1/scales1."""
+        codes, scales = send if send is not None else (self.codes, self.scales)
         if self.ef1 is not None:
-            binding.dequant_reduce_requant_ef(self.codes, self.scales, self.codes1, self.scales1,
+            binding.dequant_reduce_requant_ef(codes, scales, self.codes1, self.scales1,
                                               self.ef1, self.N, self.R, self.G, self.B,
                                               self.err_scale, self.err_beta, stream)
         else:
-            binding.dequant_reduce_requant(self.codes, self.scales, self.codes1, self.scales1,
+            binding.dequant_reduce_requant(codes, scales, self.codes1, self.scales1,
                                            self.N, self.R, self.G, self.B, stream)
 
-    def reduce_last_hop(self, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
+    def reduce_last_hop(self, stream=None, out: torch.Tensor | None = None,
+                        send=None) -> torch.Tensor:
         """The dequant-reduce into the shards (self.out unless `out` is
         given): flat, or the inter-group hop."""
         out = self.out if out is None else out
@@ -85,7 +90,8 @@ class QgzReducer:
             binding.dequant_reduce(self.codes1, self.scales1, out, self.N, self.R, self.G,
                                    self.B, self.out_scale, stream)
         else:
-            binding.dequant_reduce(self.codes, self.scales, out, self.N, self.R, 1, self.B,
+            codes, scales = send if send is not None else (self.codes, self.scales)
+            binding.dequant_reduce(codes, scales, out, self.N, self.R, 1, self.B,
                                    self.out_scale, stream)
         return out
 
@@ -111,6 +117,57 @@ class QgzReducer:
             self.step(g_dev, s)
             out_host.copy_(self.out, non_blocking=True)
         return out_host
+
+
+class DevicePipeline:
+    """Back-to-back steps with each step's reduce on a second stream, beside
+    the next step's EF-quant.
+
+    The quantization is HBM-bound and the reduce issue-bound, so running them
+    side by side lets the reduce hide under the quantization.  Ordering uses
+    events between the two streams, never a host wait (the llm.c ZeRO-2
+    review asks the same of its NCCL stream).  Two send buffers rotate:
+    step i quantizes into send[i % 2] once step i-2's reduce has read it.
+    The error buffer sees the steps in order (one quantization stream); so
+    does the first-hop error and the output (one reduce stream).
+    """
+
+    def __init__(self, red: QgzReducer):
+        self.red = red
+        self.send = [(red.codes, red.scales),
+                     (torch.empty_like(red.codes), torch.empty_like(red.scales))]
+        self.quant_stream = torch.cuda.Stream(red.device)
+        self.reduce_stream = torch.cuda.Stream(red.device)
+        self.quantized = [torch.cuda.Event() for _ in range(2)]
+        self.reduced = [torch.cuda.Event() for _ in range(2)]
+        self.count = 0
+        self.timer = None      # optional callable(kind, i, "begin"|"end", stream)
+
+    def step(self, g: torch.Tensor) -> torch.Tensor:
+        """Enqueue one step; returns red.out, valid once reduce_stream has run
+        the step (wait on it, or synchronize)."""
+        red, i = self.red, self.count
+        b = i % 2
+        qs, rs = self.quant_stream, self.reduce_stream
+        if i >= 2:
+            qs.wait_event(self.reduced[b])
+        if self.timer:
+            self.timer("quant", i, "begin", qs)
+        red.quantize(g, qs, send=self.send[b])
+        if self.timer:
+            self.timer("quant", i, "end", qs)
+        self.quantized[b].record(qs)
+        rs.wait_event(self.quantized[b])
+        if self.timer:
+            self.timer("reduce", i, "begin", rs)
+        if red.G > 1:
+            red.reduce_first_hop(rs, send=self.send[b])
+        red.reduce_last_hop(rs, send=self.send[b])
+        if self.timer:
+            self.timer("reduce", i, "end", rs)
+        self.reduced[b].record(rs)
+        self.count += 1
+        return red.out
 
 
 class HostPipeline:
