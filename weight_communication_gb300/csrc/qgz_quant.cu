@@ -47,23 +47,41 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
     constexpr int K = T / 128;
     constexpr int LPB = B >= 128 ? 32 : B / 4;  // lanes per block
     const int lane = threadIdx.x & (kWarp - 1);
-    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
-    // Warps past the end (the grid is rounded up to whole CTAs) leave at once;
-    // the comparison is 64-bit so a tile start cannot wrap around 2^32.
-    if (uint64_t(warp) * T >= geo.total) return;
-    const uint32_t tile0 = warp * uint32_t(T);
-
-    // Block owned by this lane and its position in send order.
-    const uint32_t first = tile0 + (B >= 128 ? 0u : 4u * lane);
-    const bool active = first < geo.total;
-    const uint32_t blk = first / B;
-    const uint32_t r = blk / geo.blocks_per_rank;
-    const uint32_t x0 = (blk - r * geo.blocks_per_rank) * B;  // element in rank
-    const uint32_t slice = x0 / geo.S;
-    const uint32_t off = x0 - slice * geo.S;
-    const uint32_t gq = slice / geo.L;
-    const uint32_t l = slice - gq * geo.L;
-    const uint32_t out0 = r * geo.N + (l * geo.G + gq) * geo.S + off;  // code position
+    uint32_t tile0;  // first gradient element of the warp's tile
+    uint32_t out0;   // code position of the first element of the lane's block
+    bool active;
+    if (B >= 128) {
+        // Grid x: blocks of one slice (a warp each), y: slice, z: rank -- the
+        // send position needs no division except slice -> (group, local rank).
+        const uint32_t off = (blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp) * B;
+        if (off >= geo.S) return;  // whole warp: the grid's x is rounded up
+        const uint32_t slice = blockIdx.y, r = blockIdx.z;
+        uint32_t p = slice;
+        if (geo.G > 1) {
+            const uint32_t gq = slice / geo.L;
+            p = (slice - gq * geo.L) * geo.G + gq;
+        }
+        tile0 = r * geo.N + slice * geo.S + off;
+        out0 = r * geo.N + p * geo.S + off;
+        active = true;
+    } else {
+        // 1-D grid of 128-element tiles holding 128/B blocks each.
+        const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+        // Warps past the end leave at once; the comparison is 64-bit so a tile
+        // start cannot wrap around 2^32.
+        if (uint64_t(warp) * T >= geo.total) return;
+        tile0 = warp * uint32_t(T);
+        const uint32_t first = tile0 + 4u * lane;
+        active = first < geo.total;
+        const uint32_t blk = first / B;
+        const uint32_t r = blk / geo.blocks_per_rank;
+        const uint32_t x0 = (blk - r * geo.blocks_per_rank) * B;  // element in rank
+        const uint32_t slice = x0 / geo.S;
+        const uint32_t off = x0 - slice * geo.S;
+        const uint32_t gq = slice / geo.L;
+        const uint32_t l = slice - gq * geo.L;
+        out0 = r * geo.N + (l * geo.G + gq) * geo.S + off;
+    }
 
     float c[K][4];
     float e[K][4];
@@ -136,9 +154,17 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, bool ef_bf16, 
                                      float *scales, const QgzGeometry &geo, float s,
                                      float beta, cudaStream_t stream) {
     constexpr int T = B >= 128 ? B : 128;
-    const uint32_t tiles = (geo.total + T - 1) / T;
     const uint32_t threads = 256;
-    const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
+    dim3 grid;
+    if (B >= 128) {
+        // one warp per block: x covers the S / B blocks of a slice, y the
+        // slices, z the ranks
+        const uint32_t blocks = geo.S / B;
+        grid = dim3((blocks + threads / kWarp - 1) / (threads / kWarp), geo.R, geo.R);
+    } else {
+        const uint32_t tiles = (geo.total + T - 1) / T;
+        grid = dim3((tiles + threads / kWarp - 1) / (threads / kWarp));
+    }
     const float omb = 1.0f - beta;
     if (ef == nullptr)
         ef_quant_int4_kernel<B, kEfNone><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
