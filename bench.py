@@ -284,83 +284,54 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         if timer is not None:
             timer.mark(ti, len(names))
 
-    # With an L2-resident workload the steps are timed one by one with an L2
-    # flush between them; otherwise steps run back to back, the reduce of
-    # each on a second stream beside the next quantization (DevicePipeline),
-    # unless --no-overlap.
+    # Headline: steps one after another on one stream, each kernel bracketed
+    # by events (with an L2 flush between steps for L2-resident workloads).
+    # For the others a second, shorter pass runs the steps through
+    # DevicePipeline (each reduce on a second stream beside the next
+    # quantization) and is reported beside it; --no-overlap skips that pass.
     overlap = flush is None and not args.no_overlap
     sampler = None
-
-    def serial_pass(n_steps, with_clocks):
-        nonlocal sampler
-        timer = Timer(names, n_steps)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            torch.cuda.synchronize(dev)
-            if with_clocks and args.clocks:
-                sampler = ClockSampler(dev.index or 0)
-                time.sleep(0.2)
-            barrier(dist)
-            torch.cuda.synchronize(dev)
-            t0 = time.time()
-            start.record()
-            for i in range(n_steps):
-                step(args.warmup + i, timer, i)
-                if flush is not None:
-                    flush_l2(flush)
-            end.record()
-            torch.cuda.synchronize(dev)
-            t1 = time.time()
-            barrier(dist)
-        return timer, start.elapsed_time(end) / n_steps, (t0, t1)
-
+    timer = Timer(names, args.steps)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             step(i)
             if flush is not None:
                 flush_l2(flush)
-    serial_steps = args.steps if not overlap else max(1, min(args.steps, 200))
-    timer, serial_ms, (t0, t1) = serial_pass(serial_steps, with_clocks=not overlap)
-    per_kernel = timer.per_kernel_ms()
-    overlapped = None
-    if overlap:
-        from weight_communication_gb300.qgz import DevicePipeline
-        pipe = DevicePipeline(red)
-        spans = {"quant": [[None, None] for _ in range(args.steps)],
-                 "reduce": [[None, None] for _ in range(args.steps)]}
-        for i in range(args.warmup):
-            pipe.step(batches[i % nbatch])
         torch.cuda.synchronize(dev)
-
-        def mark(kind, i, which, st):
-            if i >= pipe_base:
-                ev = torch.cuda.Event(enable_timing=True)
-                ev.record(st)
-                spans[kind][i - pipe_base][0 if which == "begin" else 1] = ev
-
-        pipe_base = pipe.count
-        pipe.timer = mark
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if args.clocks:
             sampler = ClockSampler(dev.index or 0)
             time.sleep(0.2)
         barrier(dist)
         torch.cuda.synchronize(dev)
         t0 = time.time()
-        start.record(pipe.quant_stream)
+        start.record()
         for i in range(args.steps):
-            pipe.step(batches[(args.warmup + i) % nbatch])
-        end.record(pipe.reduce_stream)
+            step(args.warmup + i, timer, i)
+            if flush is not None:
+                flush_l2(flush)
+        end.record()
         torch.cuda.synchronize(dev)
         t1 = time.time()
         barrier(dist)
-        overlapped = {k: statistics.mean(b.elapsed_time(e) for b, e in v) for k, v in spans.items()}
-        ms_local = start.elapsed_time(end) / args.steps
-    elif flush is not None:
-        # the flush is not part of the step: the step time is the kernels' span
-        ms_local = timer.step_sum_ms()
-    else:
-        ms_local = serial_ms
+    per_kernel = timer.per_kernel_ms()
+    # with a flush the step time is the kernels' span (the flush is not part of it)
+    ms_local = timer.step_sum_ms() if flush is not None else start.elapsed_time(end) / args.steps
+    overlapped = None
+    if overlap:
+        from weight_communication_gb300.qgz import DevicePipeline
+        pipe = DevicePipeline(red)
+        n_ov = max(1, min(args.steps, 200))
+        for i in range(3):
+            pipe.step(batches[i % nbatch])
+        torch.cuda.synchronize(dev)
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o0.record(pipe.quant_stream)
+        for i in range(n_ov):
+            pipe.step(batches[i % nbatch])
+        o1.record(pipe.reduce_stream)
+        torch.cuda.synchronize(dev)
+        overlapped = max_over_ranks(o0.elapsed_time(o1) / n_ov, dist, dev)
     clocks = sampler.stop(t0, t1) if sampler else None
     ms = max_over_ranks(ms_local, dist, dev)
     units = w.R * w.N
@@ -371,7 +342,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
     peak, peak_kind = measured_peaks()
     ef_bytes = 2 if ef_bf16 else 4
     efq_bytes = w.R * w.N * (2 + 2 * ef_bytes + 0.5) + w.R * w.N // w.B * 4
-    efq_ms = overlapped["quant"] if overlapped else per_kernel["ef_quant_int4"]
+    efq_ms = per_kernel["ef_quant_int4"]
     achieved = efq_bytes / (efq_ms / 1e3) / 1e9
     efq_kernel = "ef_quant_int4_bf16ef" if ef_bf16 else "ef_quant_int4"
     traffic = ncu_traffic(efq_kernel, w.name.split()[0], units) if not ef_bf16 else None
@@ -402,9 +373,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
                    "out": "bf16" if w.out_bf16 else "fp32",
                    "l2": ("flushed between steps (untimed 516 MB write)" if flush is not None
                           else f"inputs exceed L2 ({units * 10 / 1e9:.1f} GB per step)"),
-                   "steps_overlap": ("each step's reduce runs on a second stream beside the "
-                                     "next step's EF-quant (event-ordered)" if overlap
-                                     else "none: steps one after another on one stream"),
+                   "steps": "one after another on one stream",
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "kernel": efq_kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
@@ -414,11 +383,10 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         "gpu_launches": args.steps * len(names),
         "clocks": clocks,
     }
-    if overlapped:
-        line["overlapped_spans_ms"] = {"ef_quant_int4": round(overlapped["quant"], 5),
-                                       "reduce": round(overlapped["reduce"], 5)}
-        line["serial_ms_per_step"] = max_over_ranks(serial_ms, dist, dev)
-        line["kernels_from"] = f"serial pass of {serial_steps} steps (one stream)"
+    if overlapped is not None:
+        line["overlapped_ms_per_step"] = overlapped
+        line["overlapped_how"] = ("each step's reduce on a second stream beside the next "
+                                  "step's EF-quant, event-ordered (qgz.DevicePipeline)")
     if not args.no_e2e:
         line["e2e"] = run_qgz_e2e(w, red, batches[0], args, dev, dist, ws, stream)
     return line, batches[0]
@@ -476,6 +444,41 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
             "gpu_launches": args.steps}, None
 
 
+def parse_cpulist(text: str) -> list[int]:
+    """'0-3,8,10-11' -> [0, 1, 2, 3, 8, 10, 11]."""
+    cpus = []
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.extend(range(int(a), int(b) + 1))
+        else:
+            cpus.append(int(part))
+    return cpus
+
+
+def bind_host_to_gpu(dev) -> str:
+    """Run this process on the CPUs next to the GPU, so that pinned host
+    buffers allocated afterwards sit in that socket's memory.  Best effort:
+    returns what was done."""
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", str(dev.index or 0)], capture_output=True, text=True,
+                             timeout=20).stdout.strip()
+        dom, bus, rest = out.split(":")
+        path = Path(f"/sys/bus/pci/devices/{int(dom, 16):04x}:{bus.lower()}:{rest.lower()}")
+        cpus = parse_cpulist((path / "local_cpulist").read_text())
+        online = set(os.sched_getaffinity(0))
+        cpus = [c for c in cpus if c in online]
+        if not cpus:
+            return "not bound (no local CPUs)"
+        os.sched_setaffinity(0, cpus)
+        return f"bound to {len(cpus)} CPUs local to the GPU"
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return "not bound (topology unavailable)"
+
+
 def run_qgz_e2e(w, red, g_example, args, dev, dist, ws, stream):
     """Same metric through the public API with host buffers: every step copies
     its gradients host -> device (pinned), runs the kernels and copies the
@@ -484,6 +487,7 @@ def run_qgz_e2e(w, red, g_example, args, dev, dist, ws, stream):
     the serial form (copy, kernels, copy, then the next step) is reported
     beside it."""
     from weight_communication_gb300.qgz import HostPipeline
+    binding_note = bind_host_to_gpu(dev)
     g_bytes = g_example.numel() * g_example.element_size()
     n_host = 2 if g_bytes <= (2 << 30) else 1
     g_host = [g_example.cpu().pin_memory() for _ in range(n_host)]
@@ -522,7 +526,7 @@ def run_qgz_e2e(w, red, g_example, args, dev, dist, ws, stream):
     return {"value": w.R * w.N * ws / (ms / 1e3), "unit": "elements/s", "ms_per_step": ms,
             "h2d_bytes_per_step": g_bytes,
             "d2h_bytes_per_step": out_host[0].numel() * out_host[0].element_size(),
-            "pipelined": True, "serial_ms_per_step": serial_ms}
+            "pipelined": True, "serial_ms_per_step": serial_ms, "host_memory": binding_note}
 
 
 def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
@@ -728,7 +732,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
-                    help="time qgZ steps one after another on one stream")
+                    help="skip the extra pass that overlaps each reduce with the next EF-quant")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
     ap.add_argument("--scale", type=int, default=1,
                     help="divide each rank's gradient by this (profiling a smaller case)")

@@ -89,3 +89,9 @@ def test_traffic_lookup_requires_the_captured_source(tmp_path, monkeypatch):
     assert bench.ncu_traffic("ef_quant_int4", "qgz_single_hop", 400) == 4000
     assert bench.ncu_traffic("dequant_reduce", "qgz_single_hop", 400) is None
     assert bench.ncu_traffic("ef_quant_int4", "qgz_tiny", 400) is None
+
+
+def test_cpulist_parser():
+    assert bench.parse_cpulist("0-3,8,10-11\n") == [0, 1, 2, 3, 8, 10, 11]
+    assert bench.parse_cpulist("72-143") == list(range(72, 144))
+    assert bench.parse_cpulist("") == []

@@ -137,7 +137,9 @@ class DevicePipeline:
         self.send = [(red.codes, red.scales),
                      (torch.empty_like(red.codes), torch.empty_like(red.scales))]
         self.quant_stream = torch.cuda.Stream(red.device)
-        self.reduce_stream = torch.cuda.Stream(red.device)
+        # the reduce's blocks go ahead of the quantization's pending ones, so
+        # the two kernels actually share the GPU instead of queueing
+        self.reduce_stream = torch.cuda.Stream(red.device, priority=-1)
         self.quantized = [torch.cuda.Event() for _ in range(2)]
         self.reduced = [torch.cuda.Event() for _ in range(2)]
         self.count = 0
