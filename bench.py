@@ -19,6 +19,7 @@ statement of the same computation) on a bounded sample of the workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import datetime as _dt
 import hashlib
 import json
@@ -781,9 +782,17 @@ def main(argv=None):
                                                         fraction, g_example.cpu())
             del g_example
         elif name == "qwz":
-            line, _ = run_qwz(wl.QWZ_WEIGHTS, args, dev, dist, ws)
+            qw = wl.QWZ_WEIGHTS
+            if args.scale > 1:
+                n = max(qw.B, (qw.n // args.scale) // qw.B * qw.B)
+                qw = dataclasses.replace(qw, n=n, name=f"qwz sample n={n} B={qw.B}")
+            line, _ = run_qwz(qw, args, dev, dist, ws)
         else:
-            line, _ = run_sr(wl.SR_ACCUMULATE, args, dev, dist, ws)
+            sw = wl.SR_ACCUMULATE
+            if args.scale > 1:
+                n = max(8, (sw.n // args.scale) // 8 * 8)
+                sw = dataclasses.replace(sw, n=n, name=f"sr_accumulate sample n={n} x{sw.micro_steps}")
+            line, _ = run_sr(sw, args, dev, dist, ws)
         if rank == 0:
             print(json.dumps(line), flush=True)
         torch.cuda.empty_cache()
