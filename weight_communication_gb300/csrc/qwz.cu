@@ -71,23 +71,49 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
     }
 }
 
+// Warp tile of 1024 weights; lane t handles weights 512*k + 16*t + j (k < 2,
+// j < 16): a 16-byte code load per k (512 B per warp instruction), both loads
+// issued before any work so that each lane keeps 32 bytes in flight, and two
+// 16-byte bf16 stores per k.  16 consecutive weights never straddle a block
+// (B >= 32).
 __global__ void __launch_bounds__(256)
 qwz_dequant_int8_kernel(const int8_t *__restrict__ codes, const float *__restrict__ scales,
                         uint16_t *__restrict__ w_out, uint32_t n, uint32_t log2_b) {
-    const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
-    if (uint64_t(v) * 8u >= n) return;
-    const uint32_t x = v * 8u;
-    const uint2 q = ld_stream_u2(codes + x);
-    const float sc = __ldg(scales + (x >> log2_b));
-    float f[8];
-    unpack_int8x4(q.x, f);
-    unpack_int8x4(q.y, f + 4);
-    uint32_t h[8];
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
+    const int lane = threadIdx.x & (kWarp - 1);
+    if (uint64_t(warp) * 1024u >= n) return;
+    const uint32_t tile0 = warp * 1024u;
+    uint4 q[2];
+    float sc[2];
+    bool active[2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) h[j] = f32_to_bf16_bits(dequant(f[j], sc));
-    __stcs(reinterpret_cast<uint4 *>(w_out + x),
-           make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                      h[6] | (h[7] << 16)));
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t x = tile0 + 512u * k + 16u * lane;
+        active[k] = x < n;  // n is a multiple of 32, so 16 weights are all in or all out
+        if (active[k]) {
+            q[k] = ld_stream_u4(codes + x);
+            sc[k] = __ldg(scales + (x >> log2_b));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        if (!active[k]) continue;
+        const uint32_t x = tile0 + 512u * k + 16u * lane;
+        const uint32_t qw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+        uint32_t h[16];
+#pragma unroll
+        for (int wq = 0; wq < 4; ++wq) {
+            float f[4];
+            unpack_int8x4(qw[wq], f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) h[4 * wq + j] = f32_to_bf16_bits(dequant(f[j], sc[k]));
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(w_out + x);
+        __stcs(dst, make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                               h[6] | (h[7] << 16)));
+        __stcs(dst + 1, make_uint4(h[8] | (h[9] << 16), h[10] | (h[11] << 16),
+                                   h[12] | (h[13] << 16), h[14] | (h[15] << 16)));
+    }
 }
 
 template <int B>
@@ -124,7 +150,8 @@ cudaError_t launch_qwz_dequant_int8(const int8_t *codes, const float *scales, ui
     uint32_t log2_b = 0;
     while ((1u << log2_b) < uint32_t(B)) ++log2_b;
     const uint32_t threads = 256;
-    const uint32_t grid = (n / 8 + threads - 1) / threads;
+    const uint32_t warps = (n + 1023) / 1024;
+    const uint32_t grid = (warps + threads / kWarp - 1) / (threads / kWarp);
     qwz_dequant_int8_kernel<<<grid, threads, 0, stream>>>(codes, scales, w_out, n, log2_b);
     return cudaPeekAtLastError();
 }
