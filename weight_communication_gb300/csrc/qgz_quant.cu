@@ -1,4 +1,4 @@
-// qgz_quant.cu -- kernels that produce int4 codes:
+// qgz_quant.cu -- the kernel that produces the int4 send buffers:
 //   * error-feedback compensation + int4 block quantization of every rank's
 //     gradient, written in all-to-all send order (LoCo on qgZ);
 //   (the first hop of the hierarchical reduce, which requantizes, is in
