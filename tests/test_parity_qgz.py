@@ -261,3 +261,57 @@ def test_fused_step_parity(dev, R, N, B, with_ef, write_codes, out_bf16):
         else:
             ref = deq_magnitude(cc, cs, B).reshape(R, N).sum(0) * 0.5
             assert_f32_parity(to_host(out), want, ref, f"fp32 shards step {t}")
+
+
+def direct_codes_scales(R: int, N: int, B: int, seed: int):
+    """Codes drawn uniformly from [-7, 7] and scales just above 2^-126 (the
+    smallest non-zero block scale), as the exchange would deliver them: the
+    dequantized terms are all normal, but their sums cancel into the
+    subnormal range often enough to exercise gradual underflow in every
+    fp32 add of the reduce."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(-7, 8, size=R * N).astype(np.int64) & 0xF
+    codes = (q[0::2] | (q[1::2] << 4)).astype(np.uint8)
+    tiny = np.float32(np.finfo(np.float32).tiny)
+    k = rng.integers(0, 64, size=R * N // B).astype(np.float32)
+    scales = (tiny * (np.float32(1) + k * np.float32(2.0 ** -23))).astype(np.float32)
+    return codes, scales
+
+
+@pytest.mark.parametrize("R,G,B", [(8, 1, 256), (16, 2, 512), (8, 2, 256), (6, 3, 64)])
+def test_subnormal_sums_parity(dev, R, G, B):
+    N = R * B * 6
+    cc, cs = direct_codes_scales(R, N, B, seed=R * G + B)
+    cd, sd = to_dev(cc, dev), to_dev(cs, dev)
+    if G == 1:
+        out = torch.empty(N, dtype=torch.float32, device=dev)
+        binding.dequant_reduce(cd, sd, out, N, R, 1, B)
+        torch.cuda.synchronize()
+        want = ORC.dequant_reduce(cc, cs, N, R, 1, B)
+        sub = (want != 0) & (np.abs(want) < np.finfo(np.float32).tiny)
+        assert sub.sum() > 0, "the case must produce subnormal sums"
+        assert_bits_equal(to_host(out), want, "flat sums")
+    # first hop, plain and with error feedback started from subnormal errors
+    c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    binding.dequant_reduce_requant(cd, sd, c1, s1, N, R, G, B)
+    torch.cuda.synchronize()
+    oc1, os1 = ORC.dequant_reduce_requant(cc, cs, N, R, G, B)
+    assert_bits_equal(to_host(c1), oc1, "hop-1 codes")
+    assert_bits_equal(to_host(s1), os1, "hop-1 scales")
+    rng = np.random.default_rng(B)
+    e1 = (rng.standard_normal(G * N) * 1e-39).astype(np.float32)
+    e1d = to_dev(e1, dev)
+    binding.dequant_reduce_requant_ef(cd, sd, c1, s1, e1d, N, R, G, B, 1.0, 0.5)
+    torch.cuda.synchronize()
+    oc1e, os1e = ORC.dequant_reduce_requant_ef(cc, cs, N, R, G, B, e1, 1.0, 0.5)
+    assert_bits_equal(to_host(c1), oc1e, "hop-1 codes with error feedback")
+    assert_bits_equal(to_host(s1), os1e, "hop-1 scales with error feedback")
+    assert_bits_equal(to_host(e1d), e1, "hop-1 error buffer")
+    if G > 1:
+        # second hop straight from drawn codes, so that its sums underflow too
+        outf = torch.empty(N, dtype=torch.float32, device=dev)
+        c2, s2 = direct_codes_scales(1, G * N, B, seed=B + 1)
+        binding.dequant_reduce(to_dev(c2, dev), to_dev(s2, dev), outf, N, R, G, B)
+        torch.cuda.synchronize()
+        assert_bits_equal(to_host(outf), ORC.dequant_reduce(c2, s2, N, R, G, B), "hop-2 sums")
