@@ -8,7 +8,14 @@ the dequant-reduce of every destination shard.  Metric: gradient elements
 per second (R*N per step) through both kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload qgz_single_hop|qgz_tiny|qgz_hierarchical|qwz|sr|all]
+                    [--workload qgz_single_hop|qgz_fused|qgz_bf16ef|qgz_hier_ef|
+                                qgz_tiny|qgz_hierarchical|qwz|sr|all]
+
+The other workloads: the same step as one fused kernel (qgz_fused), with a
+bf16 error buffer (qgz_bf16ef), the 16-rank two-hop reduce without and with
+first-hop error feedback (qgz_hierarchical, qgz_hier_ef), the L2-resident
+4-rank step (qgz_tiny), the qwZ int8 round trip and one-pass replica (qwz),
+and the bf16 stochastic-rounding accumulate (sr).
 
 One JSON line on rank 0 (per workload).  Under torchrun each rank runs an
 independent replica on its own GPU ("weak" scaling; the simulated ranks live
