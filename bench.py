@@ -30,6 +30,7 @@ import dataclasses
 import datetime as _dt
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -235,8 +236,25 @@ def ncu_traffic(kernel: str, workload: str, units: float):
 # timed loops
 # ---------------------------------------------------------------------------
 
+def clocks_begin(args, dev):
+    """Start sampling the SM clocks before a timed region (None when off)."""
+    if not args.clocks:
+        return None
+    sampler = ClockSampler(dev.index or 0)
+    time.sleep(0.2)
+    return sampler
+
+
 def flush_l2(buf: torch.Tensor):
     buf.add_(1)
+
+
+def percentiles(xs):
+    """{median, p10, p90} of a list of times (nearest-rank percentiles)."""
+    ys = sorted(xs)
+    pick = lambda q: ys[min(len(ys) - 1, max(0, int(math.ceil(q * len(ys))) - 1))]
+    return {"median": round(statistics.median(ys), 5), "p10": round(pick(0.10), 5),
+            "p90": round(pick(0.90), 5)}
 
 
 class Timer:
@@ -256,8 +274,23 @@ class Timer:
             out[n] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in self.ev)
         return out
 
+    def per_kernel_percentiles(self):
+        """Median, 10th and 90th percentile of each kernel's launch times (ms)."""
+        out = {}
+        for j, n in enumerate(self.names):
+            out[n] = percentiles([e[j].elapsed_time(e[j + 1]) for e in self.ev])
+        return out
+
     def step_sum_ms(self):
         return statistics.mean(e[0].elapsed_time(e[-1]) for e in self.ev)
+
+
+def wire_bytes(w: wl.QgzWorkload) -> dict:
+    """Bytes each gradient element puts on the wire per exchange: a 4-bit code
+    plus its share of the block's fp32 scale, against bf16 (2 bytes) and an
+    ideal int4 with no scales (0.5)."""
+    return {"int4_blocked": 0.5 + 4 / w.B, "bf16": 2.0, "int4_no_scales": 0.5,
+            "exchanges_per_step": 2 if w.G > 1 else 1}
 
 
 def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
@@ -307,9 +340,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
             if flush is not None:
                 flush_l2(flush)
         torch.cuda.synchronize(dev)
-        if args.clocks:
-            sampler = ClockSampler(dev.index or 0)
-            time.sleep(0.2)
+        sampler = clocks_begin(args, dev)
         barrier(dist)
         torch.cuda.synchronize(dev)
         t0 = time.time()
@@ -323,6 +354,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         t1 = time.time()
         barrier(dist)
     per_kernel = timer.per_kernel_ms()
+    per_kernel_pct = timer.per_kernel_percentiles()
     # with a flush the step time is the kernels' span (the flush is not part of it)
     ms_local = timer.step_sum_ms() if flush is not None else start.elapsed_time(end) / args.steps
     overlapped = None
@@ -365,7 +397,8 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
             nsrc = w.G if w.G > 1 else w.R
             b = w.N * (nsrc * (0.5 + 4 / w.B) + (2 if w.out_bf16 else 4))
         t = per_kernel[n]
-        kernels[n] = {"ms": round(t, 5), "algorithmic_bytes": int(b),
+        kernels[n] = {"ms": round(t, 5), "ms_percentiles": per_kernel_pct[n],
+                      "algorithmic_bytes": int(b),
                       "GB/s": round(b / (t / 1e3) / 1e9, 1),
                       "frac": round(b / (t / 1e3) / 1e9 / peak, 4)}
     line = {
@@ -388,6 +421,7 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
                      "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": int(efq_bytes)},
         "kernels": kernels,
+        "wire_bytes_per_element": wire_bytes(w),
         "gpu_launches": args.steps * len(names),
         "clocks": clocks,
     }
@@ -422,13 +456,17 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
             step(i)
         torch.cuda.synchronize(dev)
         timer = Timer(names, args.steps)
+        sampler = clocks_begin(args, dev)
         barrier(dist)
+        t0 = time.time()
         for i in range(args.steps):
             timer.mark(i, 0)
             step(args.warmup + i)
             timer.mark(i, 1)
         torch.cuda.synchronize(dev)
+        t1 = time.time()
         barrier(dist)
+    clocks = sampler.stop(t0, t1) if sampler else None
     ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
     peak, kind = measured_peaks()
     b = w.R * w.N * (2 + 4 + 4 + 0.5) + w.R * w.N // w.B * 4 + w.N * (2 if w.out_bf16 else 4)
@@ -446,10 +484,13 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
                          "traffic": ncu_traffic("qgz_step_fused", "qgz_single_hop", w.R * w.N)
                          if "qgz_step_fused" in KERNEL_SOURCES else None,
                          "algorithmic_bytes": int(b)},
-            "kernels": {"qgz_step_fused": {"ms": round(ms, 5), "algorithmic_bytes": int(b),
+            "kernels": {"qgz_step_fused": {"ms": round(ms, 5),
+                                           "ms_percentiles": timer.per_kernel_percentiles()[
+                                               "qgz_step_fused"],
+                                           "algorithmic_bytes": int(b),
                                            "GB/s": round(achieved, 1),
                                            "frac": round(achieved / peak, 4)}},
-            "gpu_launches": args.steps}, None
+            "gpu_launches": args.steps, "clocks": clocks}, None
 
 
 def parse_cpulist(text: str) -> list[int]:
@@ -551,7 +592,9 @@ def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
             binding.qwz_dequant_int8(codes, scales, back, w.B, stream)
         torch.cuda.synchronize(dev)
         timer = Timer(names, args.steps)
+        sampler = clocks_begin(args, dev)
         barrier(dist)
+        t0 = time.time()
         for i in range(args.steps):
             timer.mark(i, 0)
             binding.qwz_quant_int8(wd, codes, scales, w.B, stream)
@@ -559,7 +602,9 @@ def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
             binding.qwz_dequant_int8(codes, scales, back, w.B, stream)
             timer.mark(i, 2)
         torch.cuda.synchronize(dev)
+        t1 = time.time()
         barrier(dist)
+    clocks = sampler.stop(t0, t1) if sampler else None
     # the one-pass variant that writes the codes and the bf16 replica, timed
     # on its own (not part of the round-trip step)
     rep_steps = max(1, min(args.steps, 200))
@@ -574,12 +619,14 @@ def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
         torch.cuda.synchronize(dev)
     per = timer.per_kernel_ms()
     per.update(rtimer.per_kernel_ms())
+    pct = timer.per_kernel_percentiles()
+    pct.update(rtimer.per_kernel_percentiles())
     ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
     peak, kind = measured_peaks()
     qb = w.n * (2 + 1) + w.n // w.B * 4
     kb = {"qwz_quant_int8": qb, "qwz_dequant_int8": qb,
           "qwz_quant_replica_int8": qb + 2 * w.n}
-    kernels = {n: {"ms": round(per[n], 5), "algorithmic_bytes": kb[n],
+    kernels = {n: {"ms": round(per[n], 5), "ms_percentiles": pct[n], "algorithmic_bytes": kb[n],
                    "GB/s": round(kb[n] / (per[n] / 1e3) / 1e9, 1),
                    "frac": round(kb[n] / (per[n] / 1e3) / 1e9 / peak, 4)} for n in kb}
     return {"metric": "qwZ weights/s (int8 quantize + dequantize round trip)",
@@ -594,7 +641,7 @@ def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
                          "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
                          "frac": kernels["qwz_quant_int8"]["frac"],
                          "traffic": ncu_traffic("qwz_quant_int8", "qwz", w.n)},
-            "kernels": kernels, "gpu_launches": 2 * args.steps}, None
+            "kernels": kernels, "gpu_launches": 2 * args.steps, "clocks": clocks}, None
 
 
 def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
@@ -612,7 +659,9 @@ def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
                 s.copy_(p)
         torch.cuda.synchronize(dev)
         timer = Timer(names, args.steps)
+        sampler = clocks_begin(args, dev)
         barrier(dist)
+        t0 = time.time()
         for i in range(args.steps):
             for t in range(w.micro_steps):
                 timer.mark(i, t)
@@ -621,8 +670,12 @@ def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
             for s, p in zip(srcs, pristine):      # refill the sources, untimed
                 s.copy_(p)
         torch.cuda.synchronize(dev)
+        t1 = time.time()
         barrier(dist)
+    clocks = sampler.stop(t0, t1) if sampler else None
     per = timer.per_kernel_ms()
+    launch_pct = percentiles([e[j].elapsed_time(e[j + 1]) for e in timer.ev
+                              for j in range(len(timer.names))])
     ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
     peak, kind = measured_peaks()
     b = w.n * 8
@@ -639,10 +692,11 @@ def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
                          "peak": peak, "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
                          "traffic": ncu_traffic("sr_accumulate", "sr", w.n)},
-            "kernels": {"sr_accumulate": {"ms": round(launch_ms, 5), "algorithmic_bytes": b,
+            "kernels": {"sr_accumulate": {"ms": round(launch_ms, 5), "ms_percentiles": launch_pct,
+                                          "algorithmic_bytes": b,
                                           "GB/s": round(achieved, 1),
                                           "frac": round(achieved / peak, 4)}},
-            "gpu_launches": w.micro_steps * args.steps}, None
+            "gpu_launches": w.micro_steps * args.steps, "clocks": clocks}, None
 
 
 # ---------------------------------------------------------------------------
@@ -665,6 +719,46 @@ def oracle_qgz_step(orc, w: wl.QgzWorkload, g_u16: np.ndarray, ef: np.ndarray):
     return orc.dequant_reduce(codes, scales, w.N, w.R, 1, w.B, 1.0, w.out_bf16)
 
 
+def oracle_qgz_step_threaded(orc, w: wl.QgzWorkload, g_u16: np.ndarray, ef: np.ndarray, pool):
+    """The same step with the oracle's independent pieces -- one rank's
+    quantization, one first-hop unit, one destination's reduce -- run on a
+    thread pool (the oracle's C calls release the interpreter lock)."""
+    N, R, G, B = w.N, w.R, w.G, w.B
+    parts = list(pool.map(lambda r: orc.ef_quant_int4_rank(
+        g_u16[r * N:(r + 1) * N], ef[r * N:(r + 1) * N], N, R, G, B, w.err_scale, w.err_beta),
+        range(R)))
+    codes = np.concatenate([p[0] for p in parts])
+    scales = np.concatenate([p[1] for p in parts])
+    if G > 1:
+        L = R // G
+        units = list(pool.map(lambda u: orc.dequant_reduce_requant_unit(
+            codes, scales, N, R, G, B, u // L, u % L), range(R)))
+        codes = np.concatenate([u[0] for u in units])
+        scales = np.concatenate([u[1] for u in units])
+    shards = list(pool.map(lambda k: orc.dequant_reduce_dest(
+        codes, scales, N, R, G, B, k, 1.0, w.out_bf16), range(R)))
+    return np.concatenate(shards)
+
+
+def cpu_baseline_qgz_threaded(w: wl.QgzWorkload, steps: int, fraction: int, g_u16: np.ndarray):
+    """The oracle on all host cores: ranks, first-hop units and destinations
+    spread over a thread pool of min(R, cores) threads."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    orc = oracle.get()
+    sw = qgz_sample(w, fraction)
+    cores, _ = host_cpu()
+    threads = max(1, min(sw.R, cores))
+    ef = np.zeros(sw.R * sw.N, np.float32)
+    with ThreadPoolExecutor(threads) as pool:
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            oracle_qgz_step_threaded(orc, sw, g_u16, ef, pool)
+        dt = time.perf_counter() - t0
+    return {"value": sw.R * sw.N * steps / dt, "unit": "elements/s", "cores": threads,
+            "kind": "oracle", "sample": f"the same {steps} steps, {dt:.1f} s on {threads} threads"}
+
+
 def cpu_baseline_qgz(w: wl.QgzWorkload, steps: int, fraction: int, g_full_example=None):
     """The oracle, as it stands, timed on this host on a bounded sample."""
     import oracle
@@ -684,7 +778,8 @@ def cpu_baseline_qgz(w: wl.QgzWorkload, steps: int, fraction: int, g_full_exampl
             "host_cores": cores, "cpu": model, "kind": "oracle",
             "sample": f"{steps} steps of R={sw.R} ranks x N={sw.N} elements "
                       f"(1/{fraction} of each rank's gradient; same B, G, LoCo parameters), "
-                      f"{dt:.1f} s single-threaded"}
+                      f"{dt:.1f} s single-threaded",
+            "all_cores": cpu_baseline_qgz_threaded(w, steps, fraction, g)}
 
 
 def run_reference(w_name: str, args, ws, rank):

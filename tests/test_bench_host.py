@@ -95,3 +95,35 @@ def test_cpulist_parser():
     assert bench.parse_cpulist("0-3,8,10-11\n") == [0, 1, 2, 3, 8, 10, 11]
     assert bench.parse_cpulist("72-143") == list(range(72, 144))
     assert bench.parse_cpulist("") == []
+
+
+@pytest.mark.parametrize("name", ["qgz_tiny", "qgz_hierarchical"])
+def test_threaded_oracle_step_matches_the_plain_step(name):
+    """The all-cores CPU baseline runs the oracle's per-rank, per-unit and
+    per-destination calls on threads; it must compute the same bits (and
+    leave the same error buffer) as the oracle's whole-step calls."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
+    import oracle
+    from weight_communication_gb300 import workloads as wl
+    orc = oracle.get()
+    w = bench.qgz_sample(wl.QGZ_WORKLOADS[name], 1 << 12)
+    g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
+    ef_a = np.zeros(w.R * w.N, np.float32)
+    ef_b = np.zeros(w.R * w.N, np.float32)
+    with ThreadPoolExecutor(4) as pool:
+        for _ in range(2):
+            a = bench.oracle_qgz_step(orc, w, g, ef_a)
+            b = bench.oracle_qgz_step_threaded(orc, w, g, ef_b, pool)
+            assert a.dtype == b.dtype and np.array_equal(a.view(np.uint8), b.view(np.uint8))
+            assert np.array_equal(ef_a.view(np.uint32), ef_b.view(np.uint32))
+
+
+def test_percentiles_and_wire_bytes():
+    p = bench.percentiles([5.0, 1.0, 4.0, 2.0, 3.0, 6.0, 7.0, 8.0, 9.0, 10.0])
+    assert p == {"median": 5.5, "p10": 1.0, "p90": 9.0}
+    assert bench.percentiles([2.0]) == {"median": 2.0, "p10": 2.0, "p90": 2.0}
+    from weight_communication_gb300 import workloads as wl
+    assert bench.wire_bytes(wl.QGZ_SINGLE_HOP)["int4_blocked"] == 0.515625
+    assert bench.wire_bytes(wl.QGZ_HIERARCHICAL)["int4_blocked"] == 0.5078125
+    assert bench.wire_bytes(wl.QGZ_HIERARCHICAL)["exchanges_per_step"] == 2
