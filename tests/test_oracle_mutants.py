@@ -67,6 +67,16 @@ MUTANTS = {
     "replica_skips_dequant": ("    orc_qwz_dequant_int8(codes, scales, replica, n, B);\n", "\n"),
     "fmix_constant": ("h *= 0x85EBCA6Bu;", "h *= 0x85EBCA6Cu;"),
     "fmix_shift": ("h ^= h >> 13;", "h ^= h >> 12;"),
+    "flat_reduce_reversed": ("for (int r = 0; r < R; ++r) {\n                int64_t pos = (int64_t)r * N",
+                             "for (int r = R - 1; r >= 0; --r) {\n                int64_t pos = (int64_t)r * N"),
+    "hop2_reversed": ("for (int gq = 0; gq < G; ++gq) {\n                int64_t unit",
+                      "for (int gq = G - 1; gq >= 0; --gq) {\n                int64_t unit"),
+    "hop1_reversed": ("for (int lq = 0; lq < L; ++lq) {", "for (int lq = L - 1; lq >= 0; --lq) {"),
+    "hop1_ef_compensation_sign": ("acc = acc + se1;", "acc = acc - se1;"),
+    "bf16ef_scale_dropped": ("float seh = s * eh;", "float seh = eh;"),
+    "bf16ef_residual_sign": ("float rh = c[i] - dh;", "float rh = dh - c[i];"),
+    "sr_step_ignored": ("uint32_t key = orc_mix32(orc_mix32(seed) ^ step);",
+                        "uint32_t key = orc_mix32(orc_mix32(seed));"),
 }
 
 

@@ -318,3 +318,55 @@ def test_requantization_is_idempotent(orc):
         q2, s2 = orc.quant_block(d, 7)
         assert np.array_equal(q, q2)
         assert abs(s2 - s) <= 2 * np.spacing(np.float32(s))
+
+
+# --------------------------------------------------------------------------
+# summation order, worked by hand
+# --------------------------------------------------------------------------
+# Three terms 1, 2^-24, 2^-24 added in source order: 1 + 2^-24 is a tie
+# between 1 and 1 + 2^-23 and rounds to the even 1, twice, so the sum is 1.
+# In the opposite order the two small terms first make 2^-23 and the sum is
+# 1 + 2^-23.  Every code is 1 (byte 0x11) and the block scales carry the
+# terms, so each dequantized value is exactly its scale.
+
+ONE, TINY = np.float32(1.0), np.float32(2.0**-24)
+
+
+def test_order_example_is_not_vacuous():
+    assert np.float32(np.float32(ONE + TINY) + TINY) == ONE
+    assert np.float32(ONE + np.float32(TINY + TINY)) == np.float32(1 + 2.0**-23)
+
+
+def test_flat_reduce_adds_ranks_in_order(orc):
+    R, B = 3, 32
+    N = R * B                                   # S = B: one block per chunk
+    codes = np.full(R * N // 2, 0x11, np.uint8)
+    scales = np.ones(R * N // B, np.float32)    # rank r, chunk k: block r*(N/B) + k
+    scales[[0, 3, 6]] = [ONE, TINY, TINY]       # chunk 0 of ranks 0, 1, 2
+    out = orc.dequant_reduce(codes, scales, N, R, 1, B)
+    assert np.all(out[:B] == ONE)
+    assert np.all(out[B:] == np.float32(3.0))
+
+
+def test_second_hop_adds_groups_in_order(orc):
+    R, G, B = 3, 3, 32                          # one rank per group
+    N = R * B
+    codes = np.full(G * N // 2, 0x11, np.uint8)
+    scales = np.ones(G * N // B, np.float32)    # unit gq, sub-slice g: block gq*G + g
+    scales[[0, 3, 6]] = [ONE, TINY, TINY]       # sub-slice 0 from groups 0, 1, 2
+    out = orc.dequant_reduce(codes, scales, N, R, G, B)
+    assert np.all(out[:B] == ONE)
+    assert np.all(out[B:] == np.float32(3.0))
+
+
+def test_first_hop_adds_local_ranks_in_order(orc):
+    R, G, B = 3, 1, 32                          # three local ranks, one group
+    N = R * B
+    codes = np.full(R * N // 2, 0x11, np.uint8)
+    scales = np.ones(R * N // B, np.float32)
+    scales[[0, 3, 6]] = [ONE, TINY, TINY]       # chunk 0 of local ranks 0, 1, 2
+    oc, os_ = orc.dequant_reduce_requant(codes, scales, N, R, G, B)
+    # unit 0's partial sums are all exactly 1: scale fl(1/7), every code 7
+    assert os_[0] == ONE / np.float32(7)
+    assert os_[0] != np.float32(1 + 2.0**-23) / np.float32(7)
+    assert np.all(oc[:B // 2] == 0x77)
