@@ -75,6 +75,8 @@ MUTANTS = {
     "hop1_ef_compensation_sign": ("acc = acc + se1;", "acc = acc - se1;"),
     "bf16ef_scale_dropped": ("float seh = s * eh;", "float seh = eh;"),
     "bf16ef_residual_sign": ("float rh = c[i] - dh;", "float rh = dh - c[i];"),
+    "nibble_read_unsigned": ("return v >= 8 ? v - 16 : v;", "return v;"),
+    "nibble_sign_off_by_one": ("return v >= 8 ? v - 16 : v;", "return v >= 8 ? v - 15 : v;"),
     "sr_step_ignored": ("uint32_t key = orc_mix32(orc_mix32(seed) ^ step);",
                         "uint32_t key = orc_mix32(orc_mix32(seed));"),
 }
