@@ -247,6 +247,27 @@ WC_API int wc_qwz_dequant_int8(const int8_t *codes, const float *scales,
 WC_API int wc_sr_accumulate_bf16(uint16_t *dst, uint16_t *src, int64_t n,
                                  uint32_t seed, uint32_t step, void *stream);
 
+/*
+ * wc_checked_violations -- a debugging aid with no counterpart on the pages.
+ * A library built with WC_CHECKED=1 compares every global load and store of
+ * every kernel with the extent of its buffer, as the call's sizes define it,
+ * and skips any access that would fall outside (it never traps).  This call
+ * returns the number of accesses skipped since the last reset, summed over
+ * the kernel files: 0 means every launch stayed inside its buffers.  When it
+ * is not 0, wc_last_error() names the source file and line of one of them.
+ * flags: WC_CHECK_RESET clears the records after reading them;
+ *        WC_CHECK_PROBE first launches, in each kernel file, a one-thread
+ *        kernel that fails one comparison without touching memory, so the
+ *        count includes one violation per kernel file (a self-test).
+ * Reads device memory synchronously: call it once the launches it should
+ * cover have completed (synchronize their streams first).
+ * Returns WC_EINVAL in an ordinary build or for unknown flags, WC_ECUDA if
+ * the read fails.
+ */
+#define WC_CHECK_RESET 1
+#define WC_CHECK_PROBE 2
+WC_API int wc_checked_violations(int flags);
+
 /* Message describing the calling thread's last failed call ("" if none). */
 WC_API const char *wc_last_error(void);
 

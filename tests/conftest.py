@@ -22,3 +22,17 @@ def orc():
     import oracle
     path = os.environ.get("ORACLE_LIB")
     return oracle.Oracle(path) if path else oracle.get()
+
+
+@pytest.fixture(autouse=True)
+def _checked_build_stays_in_bounds(request):
+    """With WC_EXPECT_CHECKED=1 (the library named by WC_LIBRARY is the
+    bounds-checked build), every GPU test must leave no skipped access."""
+    yield
+    if os.environ.get("WC_EXPECT_CHECKED") != "1" or request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    from weight_communication_gb300 import binding
+    torch.cuda.synchronize()
+    n = binding.checked_violations(reset=True)
+    assert n == 0, binding.last_error()

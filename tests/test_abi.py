@@ -154,3 +154,21 @@ def test_bf16ef_and_replica_argument_errors(lib):
     assert q(FAKE, FAKE, FAKE, None, 4096, 2048, None) == binding.WC_EINVAL
     assert q(FAKE, FAKE, FAKE, MIS, 4096, 2048, None) == binding.WC_EALIGN
     assert q(FAKE, FAKE, FAKE, FAKE, 4000, 2048, None) == binding.WC_EINVAL
+
+
+def test_checked_violations_needs_a_checked_build(lib):
+    """The ordinary library has no bounds checks: the debugging call says so
+    (and rejects unknown flags) without touching the GPU."""
+    assert lib.wc_checked_violations(0) == binding.WC_EINVAL
+    assert b"without checks" in lib.wc_last_error()
+    assert lib.wc_checked_violations(4) == binding.WC_EINVAL
+    assert b"unknown flags" in lib.wc_last_error()
+
+
+def test_checked_build_exports_the_same_symbols():
+    """The bounds-checked library (WC_CHECKED=1) builds from the same sources
+    and exports every declared entry point."""
+    lib_path = build.build(checked=True)
+    raw = ctypes.CDLL(str(lib_path))
+    for n in _declared():
+        assert hasattr(raw, n), n

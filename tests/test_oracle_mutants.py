@@ -89,7 +89,9 @@ def _run_mutant(name, tmp: Path):
     mpath = tmp / f"{name}.c"
     mpath.write_text(src.replace(old, new))
     lib = oracle.build(mpath, tmp / f"lib{name}.so", extra=["-w"])
-    env = dict(os.environ, ORACLE_LIB=str(lib))
+    # one thread per child: the children already run one per core
+    env = dict(os.environ, ORACLE_LIB=str(lib), OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               OPENBLAS_NUM_THREADS="1")
     proc = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                            *PIN_FILES], cwd=ROOT, env=env, capture_output=True, text=True,
                           timeout=900)

@@ -9,6 +9,7 @@ is raised.
 from __future__ import annotations
 
 import ctypes
+import os
 from pathlib import Path
 
 import torch
@@ -36,6 +37,7 @@ SIGNATURES = {
     "wc_qwz_quant_replica_int8": [_P, _P, _P, _P, _I64, _I, _P],
     "wc_qwz_dequant_int8": [_P, _P, _P, _I64, _I, _P],
     "wc_sr_accumulate_bf16": [_P, _P, _I64, _U32, _U32, _P],
+    "wc_checked_violations": [_I],
     "wc_last_error": [],
     "wc_version": [],
 }
@@ -51,7 +53,10 @@ _lib: ctypes.CDLL | None = None
 
 
 def library_path() -> Path:
-    return _build.LIB
+    """The in-tree libwc.so, or the file named by the WC_LIBRARY environment
+    variable (for instance the bounds-checked build)."""
+    env = os.environ.get("WC_LIBRARY")
+    return Path(env) if env else _build.LIB
 
 
 def load(path: str | Path | None = None) -> ctypes.CDLL:
@@ -79,6 +84,21 @@ def last_error() -> str:
 
 def version() -> int:
     return load().wc_version()
+
+
+WC_CHECK_RESET, WC_CHECK_PROBE = 1, 2
+
+
+def checked_violations(reset: bool = False, probe: bool = False) -> int:
+    """wc_checked_violations: accesses a checked build skipped (synchronize
+    first); probe adds one deliberate violation per kernel file first.
+    Raises WcError on an ordinary build."""
+    lib = load()
+    rc = lib.wc_checked_violations((WC_CHECK_RESET if reset else 0) |
+                                   (WC_CHECK_PROBE if probe else 0))
+    if rc < 0:
+        raise WcError("wc_checked_violations", rc, lib.wc_last_error().decode())
+    return rc
 
 
 def _call(name: str, *args) -> None:

@@ -256,4 +256,41 @@ WC_API int wc_sr_accumulate_bf16(uint16_t *dst, uint16_t *src, int64_t n, uint32
                      fn);
 }
 
+WC_API int wc_checked_violations(int flags) {
+    static const char *fn = "wc_checked_violations";
+    if (flags & ~(WC_CHECK_RESET | WC_CHECK_PROBE))
+        return fail(WC_EINVAL, "%s: unknown flags 0x%x", fn, unsigned(flags));
+#if defined(WC_CHECKED) && WC_CHECKED
+    struct Reader {
+        const char *file;
+        cudaError_t (*read)(wc::CheckRecord *, bool, bool);
+    };
+    static const Reader readers[] = {
+        {"qgz_quant.cu", wc::check_record_qgz_quant}, {"qgz_reduce.cu", wc::check_record_qgz_reduce},
+        {"qgz_hop1.cu", wc::check_record_qgz_hop1},   {"qgz_fused.cu", wc::check_record_qgz_fused},
+        {"qwz.cu", wc::check_record_qwz},
+    };
+    uint64_t total = 0;
+    const char *first_file = nullptr;
+    unsigned int first_line = 0;
+    for (const Reader &r : readers) {
+        wc::CheckRecord rec = {0u, 0u};
+        const cudaError_t e = r.read(&rec, (flags & WC_CHECK_RESET) != 0,
+                                     (flags & WC_CHECK_PROBE) != 0);
+        if (e != cudaSuccess) return from_cuda(e, fn);
+        if (rec.count != 0 && first_file == nullptr) {
+            first_file = r.file;
+            first_line = rec.first_line;
+        }
+        total += rec.count;
+    }
+    if (total == 0) return 0;
+    fail(WC_OK, "%s: %llu accesses skipped, one of them in %s line %u", fn,
+         (unsigned long long)total, first_file, first_line);
+    return total > 0x7FFFFFFFull ? 0x7FFFFFFF : int(total);
+#else
+    return fail(WC_EINVAL, "%s: this library was built without checks (WC_CHECKED=1)", fn);
+#endif
+}
+
 }  // extern "C"

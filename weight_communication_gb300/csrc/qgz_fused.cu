@@ -42,8 +42,12 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[k][j] = 0.0f;
         const uint32_t x = x0 + 128u * k + 4u * lane;  // rank 0
-        gv[k] = ld_stream_u2(g + x);
-        ev[k] = HAS_EF ? ld_stream_f4(ef + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+        gv[k] = make_uint2(0u, 0u);
+        ev[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
+            gv[k] = ld_stream_u2(g + x);
+            if (HAS_EF) ev[k] = ld_stream_f4(ef + x);
+        }
     }
 
     for (uint32_t r = 0; r < geo.R; ++r) {
@@ -55,8 +59,12 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const uint32_t x = xr + geo.N + 128u * k + 4u * lane;
-                gn[k] = ld_stream_u2(g + x);
-                en[k] = HAS_EF ? ld_stream_f4(ef + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+                gn[k] = make_uint2(0u, 0u);
+                en[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
+                    gn[k] = ld_stream_u2(g + x);
+                    if (HAS_EF) en[k] = ld_stream_f4(ef + x);
+                }
             }
         }
         float c[K][4];
@@ -92,11 +100,13 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
                     o[j] = __fadd_rn(__fmul_rn(beta, e[k][j]),
                                      __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));
             }
+            if (!WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) continue;
             if (HAS_EF) __stcs(reinterpret_cast<float4 *>(ef + x), eo);
             if (WRITE_CODES)
                 __stcs(reinterpret_cast<unsigned short *>(codes + x / 2), (unsigned short)packed);
         }
-        if (WRITE_CODES && lane == 0) __stcs(scales + xr / B, bs.scale);
+        if (WRITE_CODES && lane == 0 && WC_IN_BOUNDS(xr / B < geo.total / B))
+            __stcs(scales + xr / B, bs.scale);
         if (r + 1 < geo.R) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -109,6 +119,7 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const uint32_t x = x0 + 128u * k + 4u * lane;  // destination-major output = slice order
+        if (!WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.N)) continue;
         if (OUT_BF16) {
             const uint32_t h0 = f32_to_bf16_bits(__fmul_rn(acc[k][0], out_scale));
             const uint32_t h1 = f32_to_bf16_bits(__fmul_rn(acc[k][1], out_scale));
@@ -158,6 +169,8 @@ static cudaError_t launch_fused_b(const uint16_t *g, float *ef, uint8_t *codes, 
     return launch_fused_3<B, false, false>(g, ef, codes, scales, geo, s, beta, out_scale, out,
                                            out_bf16, stream);
 }
+
+WC_CHECK_RECORD_READER(check_record_qgz_fused)
 
 cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
                                   const QgzGeometry &geo, int B, float s, float beta,

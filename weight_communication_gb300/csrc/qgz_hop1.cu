@@ -79,8 +79,10 @@ __device__ __forceinline__ void store_words(uint8_t *p, const uint32_t w[W]) {
 // E (a multiple of 8) consecutive values of one lane, in place: compensation
 // c = p + s*e1 (HAS_EF), absmax over the LPB-lane group that holds the block,
 // int4 codes to out_codes at code position o, the error update, the scale.
+// out_ok (false only in a checked build, for a lane whose outputs would lie
+// outside the G*N outputs) skips every access of the lane.
 template <int E, int LPB, bool HAS_EF, int B>
-__device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, int lane,
+__device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, bool out_ok, int lane,
                                                 uint8_t *__restrict__ out_codes,
                                                 float *__restrict__ out_scales,
                                                 float *__restrict__ ef1, float s, float beta,
@@ -89,7 +91,7 @@ __device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, int lane
     if (HAS_EF) {
 #pragma unroll
         for (int q = 0; q < E / 4; ++q) {
-            const float4 v = ld_stream_f4(ef1 + o + 4 * q);
+            const float4 v = out_ok ? ld_stream_f4(ef1 + o + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
             e[4 * q] = v.x;
             e[4 * q + 1] = v.y;
             e[4 * q + 2] = v.z;
@@ -116,8 +118,8 @@ __device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, int lane
         }
         words[wq] = packed;
     }
-    store_words<E / 8>(out_codes + o / 2, words);
-    if (HAS_EF) {
+    if (out_ok) store_words<E / 8>(out_codes + o / 2, words);
+    if (HAS_EF && out_ok) {
 #pragma unroll
         for (int qd = 0; qd < E / 4; ++qd) {
             float4 v;
@@ -132,7 +134,7 @@ __device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, int lane
             __stcs(reinterpret_cast<float4 *>(ef1 + o + 4 * qd), v);
         }
     }
-    if ((lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
+    if (out_ok && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
 }
 
 template <int B, int L, bool HAS_EF>
@@ -157,8 +159,14 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
     float sc[L];
 #pragma unroll
     for (int t = 0; t < L; ++t) {
-        load_words<W>(cp + size_t(t) * cstride, w[t]);
-        sc[t] = __ldg(sp + size_t(t) * sstride);
+#pragma unroll
+        for (int q = 0; q < W; ++q) w[t][q] = 0u;
+        sc[t] = 0.0f;
+        // source t's E codes lie inside the R ranks' N codes each
+        if (WC_IN_BOUNDS(uint64_t(pos0) + uint64_t(t) * geo.N + E <= geo.total)) {
+            load_words<W>(cp + size_t(t) * cstride, w[t]);
+            sc[t] = __ldg(sp + size_t(t) * sstride);
+        }
     }
     float p[E];
 #pragma unroll
@@ -173,7 +181,8 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
             for (int j = 0; j < 8; ++j) p[8 * wq + j] = __fadd_rn(p[8 * wq + j], dequant(f[j], sc[t]));
         }
     }
-    requantize_lane<E, kWarp, HAS_EF, B>(p, o, lane, out_codes, out_scales, ef1, s, beta,
+    const bool out_ok = WC_IN_BOUNDS(uint64_t(o) + E <= uint64_t(geo.G) * geo.N);
+    requantize_lane<E, kWarp, HAS_EF, B>(p, o, out_ok, lane, out_codes, out_scales, ef1, s, beta,
                                          one_minus_beta);
 }
 
@@ -210,6 +219,10 @@ hop1_general_kernel(const uint8_t *__restrict__ codes, const float *__restrict__
             e[k][j] = 0.0f;
         }
         if (!active[k]) continue;
+        if (!WC_IN_BOUNDS(uint64_t(o) + 8 <= total_out)) {
+            active[k] = false;  // checked builds: the lane's outputs are not all there
+            continue;
+        }
         const uint32_t pos0 = hop1_source(geo, o);
         const uint8_t *cp = codes + pos0 / 2;
         const float *sp = scales + pos0 / B;
@@ -219,7 +232,10 @@ hop1_general_kernel(const uint8_t *__restrict__ codes, const float *__restrict__
             const uint32_t nb = min(8u, geo.L - l0);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                if (t < nb) {
+                w[t] = 0u;
+                sc[t] = 0.0f;
+                if (t < nb &&
+                    WC_IN_BOUNDS(uint64_t(pos0) + uint64_t(l0 + t) * geo.N + 8 <= geo.total)) {
                     w[t] = __ldcs(reinterpret_cast<const unsigned int *>(cp + size_t(l0 + t) * cstride));
                     sc[t] = __ldg(sp + size_t(l0 + t) * sstride);
                 }
@@ -342,6 +358,8 @@ static cudaError_t launch_ef(const uint8_t *codes, const float *scales, uint8_t 
     }
     return cudaPeekAtLastError();
 }
+
+WC_CHECK_RECORD_READER(check_record_qgz_hop1)
 
 cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *scales,
                                           uint8_t *out_codes, float *out_scales,

@@ -90,7 +90,7 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         const uint32_t x = tile0 + 128u * k + 4u * lane;
         uint2 gv = make_uint2(0u, 0u);
         float4 ev = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (active) {
+        if (active && WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
             gv = ld_stream_u2(g + x);
             if (EF == kEfF32) ev = ld_stream_f4(ef + x);
             if (EF == kEfBf16) {
@@ -128,7 +128,8 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         }
         const uint32_t in_blk = B >= 128 ? 128u * k + 4u * lane : (4u * lane) % B;
         const uint32_t pos = out0 + in_blk;
-        __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2), (unsigned short)packed);
+        if (WC_IN_BOUNDS(uint64_t(pos) + 4 <= geo.total))
+            __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2), (unsigned short)packed);
         if (HAS_EF) {
             float4 ev;
             float *o = &ev.x;
@@ -139,6 +140,7 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                                  __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));
             }
             const uint32_t x = tile0 + 128u * k + 4u * lane;
+            if (!WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) continue;
             if (EF == kEfF32) __stcs(reinterpret_cast<float4 *>(ef + x), ev);
             if (EF == kEfBf16)
                 __stcs(reinterpret_cast<uint2 *>(ef16 + x),
@@ -146,7 +148,8 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                                   uint32_t(f32_to_bf16_bits(ev.z)) | (uint32_t(f32_to_bf16_bits(ev.w)) << 16)));
         }
     }
-    if ((lane & (LPB - 1)) == 0) __stcs(scales + out0 / B, bs.scale);
+    if ((lane & (LPB - 1)) == 0 && WC_IN_BOUNDS(out0 / B < geo.total / B))
+        __stcs(scales + out0 / B, bs.scale);
 }
 
 template <int B>
@@ -177,6 +180,8 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, bool ef_bf16, 
                                                                        s, beta, omb);
     return cudaPeekAtLastError();
 }
+
+WC_CHECK_RECORD_READER(check_record_qgz_quant)
 
 cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
                                  float *scales, const QgzGeometry &geo, int B, float s,

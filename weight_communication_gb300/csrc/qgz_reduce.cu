@@ -75,6 +75,18 @@ __device__ __forceinline__ uint32_t source_base(const QgzGeometry &geo, uint32_t
     return chunk * geo.S + i;
 }
 
+// Checked builds: source t's 16 codes (and so its scale) lie inside the
+// source buffers, R of N codes each for the flat reduce, G for the second hop.
+__device__ __forceinline__ bool source_in_bounds(const QgzGeometry &geo, uint32_t base,
+                                                 uint32_t t) {
+    const uint64_t ncodes = uint64_t(geo.G > 1 ? geo.G : geo.R) * geo.N;
+    return uint64_t(base) + uint64_t(t) * geo.N + kOutPerThread <= ncodes;
+}
+
+__device__ __forceinline__ bool output_in_bounds(const QgzGeometry &geo, uint32_t k, uint32_t i) {
+    return uint64_t(k) * geo.S + i + kOutPerThread <= geo.N;
+}
+
 template <int NSRC, bool OUT_BF16>
 __global__ void __launch_bounds__(256)
 dequant_reduce_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
@@ -94,15 +106,20 @@ dequant_reduce_fixed_kernel(const uint8_t *__restrict__ codes, const float *__re
     float sc[NSRC];
 #pragma unroll
     for (int t = 0; t < NSRC; ++t) {
-        w[t] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride));
-        sc[t] = __ldg(sp + size_t(t) * sstride);
+        w[t] = make_uint2(0u, 0u);
+        sc[t] = 0.0f;
+        if (WC_IN_BOUNDS(source_in_bounds(geo, base, t))) {
+            w[t] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride));
+            sc[t] = __ldg(sp + size_t(t) * sstride);
+        }
     }
     float acc[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
 #pragma unroll
     for (int t = 0; t < NSRC; ++t) accumulate16(w[t], sc[t], acc);
-    store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
+    if (WC_IN_BOUNDS(output_in_bounds(geo, k, i)))
+        store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
 }
 
 template <bool OUT_BF16>
@@ -129,16 +146,22 @@ dequant_reduce_loop_kernel(const uint8_t *__restrict__ codes, const float *__res
         float sc[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            w[u] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t + u) * cstride));
-            sc[u] = __ldg(sp + size_t(t + u) * sstride);
+            w[u] = make_uint2(0u, 0u);
+            sc[u] = 0.0f;
+            if (WC_IN_BOUNDS(source_in_bounds(geo, base, t + u))) {
+                w[u] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t + u) * cstride));
+                sc[u] = __ldg(sp + size_t(t + u) * sstride);
+            }
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) accumulate16(w[u], sc[u], acc);
     }
     for (; t < nsrc; ++t)
-        accumulate16(__ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride)),
-                     __ldg(sp + size_t(t) * sstride), acc);
-    store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
+        if (WC_IN_BOUNDS(source_in_bounds(geo, base, t)))
+            accumulate16(__ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride)),
+                         __ldg(sp + size_t(t) * sstride), acc);
+    if (WC_IN_BOUNDS(output_in_bounds(geo, k, i)))
+        store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
 }
 
 template <int NSRC, bool OUT_BF16>
@@ -167,6 +190,8 @@ static void launch_any(const uint8_t *codes, const float *scales, const QgzGeome
     }
 #undef WC_FIXED
 }
+
+WC_CHECK_RECORD_READER(check_record_qgz_reduce)
 
 cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
                                   const QgzGeometry &geo, int B, float out_scale, void *out,

@@ -36,7 +36,7 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const uint32_t x = tile0 + 256u * k + 8u * lane;
-        active[k] = x < n;
+        active[k] = x < n && WC_IN_BOUNDS(uint64_t(x) + 8 <= n);
         raw[k] = active[k] ? ld_stream_u4(w + x) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t *h = &raw[k].x;
 #pragma unroll
@@ -67,7 +67,8 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
         __stcs(reinterpret_cast<uint2 *>(codes + x), make_uint2(word[0], word[1]));
         if (REPLICA)
             __stcs(reinterpret_cast<uint4 *>(replica + x), make_uint4(rep[0], rep[1], rep[2], rep[3]));
-        if (k == 0 && (lane & (LPB - 1)) == 0) __stcs(scales + x / B, bs.scale);
+        if (k == 0 && (lane & (LPB - 1)) == 0 && WC_IN_BOUNDS(x / B < n / B))
+            __stcs(scales + x / B, bs.scale);
     }
 }
 
@@ -89,7 +90,9 @@ qwz_dequant_int8_kernel(const int8_t *__restrict__ codes, const float *__restric
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const uint32_t x = tile0 + 512u * k + 16u * lane;
-        active[k] = x < n;  // n is a multiple of 32, so 16 weights are all in or all out
+        // n is a multiple of 32, so 16 weights are all in or all out
+        active[k] = x < n && WC_IN_BOUNDS(uint64_t(x) + 16 <= n) &&
+                    WC_IN_BOUNDS((x >> log2_b) < (n >> log2_b));
         if (active[k]) {
             q[k] = ld_stream_u4(codes + x);
             sc[k] = __ldg(scales + (x >> log2_b));
@@ -129,6 +132,8 @@ static cudaError_t launch_qwz_quant_b(const uint16_t *w, int8_t *codes, float *s
         qwz_quant_int8_kernel<B, false><<<grid, threads, 0, stream>>>(w, codes, scales, replica, n);
     return cudaPeekAtLastError();
 }
+
+WC_CHECK_RECORD_READER(check_record_qwz)
 
 cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
                                   uint16_t *replica, uint32_t n, int B, cudaStream_t stream) {

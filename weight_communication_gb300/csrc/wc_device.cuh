@@ -11,11 +11,61 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "wc_internal.h"
+
 namespace wc {
 
 constexpr int kWarp = 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr float kMinNormal = 1.17549435082228750797e-38f;  // 2^-126
+
+// Checked builds (compiled with -DWC_CHECKED=1): before every global load or
+// store a kernel compares the access with the extent of its buffer, as the
+// call's sizes define it.  WC_IN_BOUNDS(ok) is that comparison.  A failure
+// counts one violation in this source file's record, keeps the first failing
+// line, and skips the access, so a checked kernel never touches memory
+// outside its buffers and never traps.  The host reads and clears the records
+// through wc_checked_violations().  In ordinary builds WC_IN_BOUNDS(ok) is
+// the constant true and the comparison is not compiled.
+#ifndef WC_CHECKED
+#define WC_CHECKED 0
+#endif
+
+#if WC_CHECKED
+static __device__ CheckRecord g_check_record;
+
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned int line) {
+    if (!ok) {
+        atomicAdd(&g_check_record.count, 1u);
+        atomicCAS(&g_check_record.first_line, 0u, line);
+    }
+    return ok;
+}
+#define WC_IN_BOUNDS(ok) ::wc::in_bounds((ok), __LINE__)
+
+// Host reader of this source file's record (one per file: the record is
+// file-local device memory).  probe first launches a one-thread kernel of
+// this file that fails one comparison and touches no memory, to show that a
+// violation reaches the host.
+#define WC_CHECK_RECORD_READER(name)                                                    \
+    __global__ void name##_probe() { (void)WC_IN_BOUNDS(false); }                       \
+    cudaError_t name(CheckRecord *out, bool reset, bool probe) {                        \
+        if (probe) {                                                                     \
+            name##_probe<<<1, 1>>>();                                                    \
+            const cudaError_t p = cudaGetLastError();                                    \
+            if (p != cudaSuccess) return p;                                              \
+        }                                                                                \
+        cudaError_t e = cudaMemcpyFromSymbol(out, g_check_record, sizeof(CheckRecord));  \
+        if (e == cudaSuccess && reset) {                                                 \
+            const CheckRecord zero = {0u, 0u};                                           \
+            e = cudaMemcpyToSymbol(g_check_record, &zero, sizeof(CheckRecord));          \
+        }                                                                                \
+        return e;                                                                        \
+    }
+#else
+#define WC_IN_BOUNDS(ok) true
+#define WC_CHECK_RECORD_READER(name)
+#endif
 
 // bf16 bit pattern -> fp32 (exact: a bf16 is the upper half of a binary32).
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) {

@@ -44,4 +44,20 @@ cudaError_t launch_sr_accumulate(uint16_t *dst, uint16_t *src, uint32_t n, uint3
                                  uint32_t step, cudaStream_t stream);
 uint32_t sr_key(uint32_t seed, uint32_t step);
 
+// Violation record of one source file's kernels in a checked build (see
+// WC_IN_BOUNDS in wc_device.cuh).  sr_accumulate.cu has none: its kernel
+// tests every access against the element count as part of its own logic.
+struct CheckRecord {
+    unsigned int count;       // accesses skipped since the last reset
+    unsigned int first_line;  // source line of the first one (0: none)
+};
+
+#if defined(WC_CHECKED) && WC_CHECKED
+cudaError_t check_record_qgz_quant(CheckRecord *out, bool reset, bool probe);
+cudaError_t check_record_qgz_reduce(CheckRecord *out, bool reset, bool probe);
+cudaError_t check_record_qgz_hop1(CheckRecord *out, bool reset, bool probe);
+cudaError_t check_record_qgz_fused(CheckRecord *out, bool reset, bool probe);
+cudaError_t check_record_qwz(CheckRecord *out, bool reset, bool probe);
+#endif
+
 }  // namespace wc
