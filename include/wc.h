@@ -23,9 +23,11 @@
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers to memory the caller allocated and owns;
  *     the library allocates nothing, frees nothing and never synchronizes
- *     the host.  Every call is asynchronous on `stream` (a cudaStream_t; NULL
- *     is the legacy default stream) and reads/writes its buffers only in
- *     stream order.
+ *     the host (the debugging call wc_checked_violations excepted).  Every
+ *     call is asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and reads/writes its buffers only in stream order.
+ *   - Kernels launch on the calling thread's current device: the pointers
+ *     and the stream must belong to it.
  *   - bf16 values are passed as uint16_t bit patterns.
  *   - Every device pointer must be 16-byte aligned (WC_EALIGN otherwise).
  *   - Buffers must not overlap unless an entry point says so.

@@ -101,9 +101,12 @@ def checked_violations(reset: bool = False, probe: bool = False) -> int:
     return rc
 
 
-def _call(name: str, *args) -> None:
+def _call(device: torch.device, name: str, *args) -> None:
+    """Calls the entry point with the tensors' GPU as the current device (the
+    kernels launch on the current device)."""
     lib = load()
-    rc = getattr(lib, name)(*args)
+    with torch.cuda.device(device):
+        rc = getattr(lib, name)(*args)
     if rc != WC_OK:
         raise WcError(name, rc, lib.wc_last_error().decode())
 
@@ -135,7 +138,7 @@ def ef_quant_int4(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor,
     """wc_ef_quant_int4: g bf16 [R*N], ef fp32 [R*N] (in place) or None,
     codes uint8 [R*N/2], scales fp32 [R*N/B] -- all written in send order."""
     d = g.device
-    _call("wc_ef_quant_int4", _dev(g, "g", torch.bfloat16, R * N, d),
+    _call(d, "wc_ef_quant_int4", _dev(g, "g", torch.bfloat16, R * N, d),
           _dev(ef, "ef", torch.float32, R * N, d), _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
           _stream(g, stream))
@@ -154,7 +157,7 @@ def dequant_reduce(codes: torch.Tensor, scales: torch.Tensor, out: torch.Tensor,
         od = WC_BF16
     else:
         raise TypeError("out must be float32 or bfloat16")
-    _call("wc_dequant_reduce", _dev(codes, "codes", torch.uint8, span // 2, d),
+    _call(d, "wc_dequant_reduce", _dev(codes, "codes", torch.uint8, span // 2, d),
           _dev(scales, "scales", torch.float32, span // B, d), N, R, G, B, out_scale,
           _dev(out, "out", out.dtype, N, d), od, _stream(codes, stream))
 
@@ -165,7 +168,7 @@ def dequant_reduce_requant(codes: torch.Tensor, scales: torch.Tensor, out_codes:
     """wc_dequant_reduce_requant: first hop; out_codes uint8 [G*N/2],
     out_scales fp32 [G*N/B] (unit u = g*L + l holds G*S values)."""
     d = codes.device
-    _call("wc_dequant_reduce_requant", _dev(codes, "codes", torch.uint8, R * N // 2, d),
+    _call(d, "wc_dequant_reduce_requant", _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B,
           _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
           _dev(out_scales, "out_scales", torch.float32, G * N // B, d), _stream(codes, stream))
@@ -178,7 +181,7 @@ def dequant_reduce_requant_ef(codes: torch.Tensor, scales: torch.Tensor, out_cod
     """wc_dequant_reduce_requant_ef: first hop with error feedback on the
     requantization; ef1 fp32 [G*N] updated in place."""
     d = codes.device
-    _call("wc_dequant_reduce_requant_ef", _dev(codes, "codes", torch.uint8, R * N // 2, d),
+    _call(d, "wc_dequant_reduce_requant_ef", _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B,
           _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
           _dev(out_scales, "out_scales", torch.float32, G * N // B, d),
@@ -198,7 +201,7 @@ def qgz_step_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor
         od = WC_BF16
     else:
         raise TypeError("out must be float32 or bfloat16")
-    _call("wc_qgz_step_fused", _dev(g, "g", torch.bfloat16, R * N, d),
+    _call(d, "wc_qgz_step_fused", _dev(g, "g", torch.bfloat16, R * N, d),
           _dev(ef, "ef", torch.float32, R * N, d),
           _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, B, err_scale, err_beta,
@@ -209,7 +212,7 @@ def qwz_quant_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, B
                    stream=None) -> None:
     n = w.numel()
     d = w.device
-    _call("wc_qwz_quant_int8", _dev(w, "w", torch.bfloat16, n, d),
+    _call(d, "wc_qwz_quant_int8", _dev(w, "w", torch.bfloat16, n, d),
           _dev(codes, "codes", torch.int8, n, d), _dev(scales, "scales", torch.float32, n // B, d),
           n, B, _stream(w, stream))
 
@@ -219,7 +222,7 @@ def ef_quant_int4_bf16ef(g: torch.Tensor, ef16: torch.Tensor, codes: torch.Tenso
                          err_scale: float = 1.0, err_beta: float = 0.0, stream=None) -> None:
     """wc_ef_quant_int4_bf16ef: as ef_quant_int4 with a bf16 error buffer."""
     d = g.device
-    _call("wc_ef_quant_int4_bf16ef", _dev(g, "g", torch.bfloat16, R * N, d),
+    _call(d, "wc_ef_quant_int4_bf16ef", _dev(g, "g", torch.bfloat16, R * N, d),
           _dev(ef16, "ef16", torch.bfloat16, R * N, d),
           _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
@@ -231,7 +234,7 @@ def qwz_quant_replica_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.T
     """wc_qwz_quant_replica_int8: codes, scales and the bf16 replica in one pass."""
     n = w.numel()
     d = w.device
-    _call("wc_qwz_quant_replica_int8", _dev(w, "w", torch.bfloat16, n, d),
+    _call(d, "wc_qwz_quant_replica_int8", _dev(w, "w", torch.bfloat16, n, d),
           _dev(codes, "codes", torch.int8, n, d), _dev(scales, "scales", torch.float32, n // B, d),
           _dev(replica, "replica", torch.bfloat16, n, d), n, B, _stream(w, stream))
 
@@ -240,7 +243,7 @@ def qwz_dequant_int8(codes: torch.Tensor, scales: torch.Tensor, w_out: torch.Ten
                      stream=None) -> None:
     n = codes.numel()
     d = codes.device
-    _call("wc_qwz_dequant_int8", _dev(codes, "codes", torch.int8, n, d),
+    _call(d, "wc_qwz_dequant_int8", _dev(codes, "codes", torch.int8, n, d),
           _dev(scales, "scales", torch.float32, n // B, d),
           _dev(w_out, "w_out", torch.bfloat16, n, d), n, B, _stream(codes, stream))
 
@@ -250,6 +253,6 @@ def sr_accumulate_bf16(dst: torch.Tensor, src: torch.Tensor, seed: int, step: in
     """dst <- SR_bf16(dst + src) in place; src <- 0."""
     n = dst.numel()
     d = dst.device
-    _call("wc_sr_accumulate_bf16", _dev(dst, "dst", torch.bfloat16, n, d),
+    _call(d, "wc_sr_accumulate_bf16", _dev(dst, "dst", torch.bfloat16, n, d),
           _dev(src, "src", torch.bfloat16, n, d), n, seed & 0xFFFFFFFF, step & 0xFFFFFFFF,
           _stream(dst, stream))
