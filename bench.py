@@ -419,7 +419,9 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         "roofline": {"bound": "hbm", "kernel": efq_kernel, "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"hbm_gbs of {peak_kind}", "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": int(efq_bytes)},
+                     "traffic": traffic, "algorithmic_bytes": int(efq_bytes),
+                     "dram_GB/s": (round(traffic / (efq_ms / 1e3) / 1e9, 1)
+                                   if traffic is not None else None)},
         "kernels": kernels,
         "wire_bytes_per_element": wire_bytes(w),
         "gpu_launches": args.steps * len(names),
@@ -759,8 +761,32 @@ def cpu_baseline_qgz_threaded(w: wl.QgzWorkload, steps: int, fraction: int, g_u1
             "kind": "oracle", "sample": f"the same {steps} steps, {dt:.1f} s on {threads} threads"}
 
 
-def cpu_baseline_qgz(w: wl.QgzWorkload, steps: int, fraction: int, g_full_example=None):
-    """The oracle, as it stands, timed on this host on a bounded sample."""
+def gpu_parity_on_sample(sw: wl.QgzWorkload, g_u16: np.ndarray, steps: int,
+                         want_out: np.ndarray, want_ef: np.ndarray, dev) -> dict:
+    """The CUDA path on the CPU baseline's sample: the same steps on the same
+    bytes, its last shards and error buffers compared bit for bit with the
+    oracle's."""
+    from weight_communication_gb300.qgz import QgzReducer
+    red = QgzReducer(sw.N, sw.R, sw.G, sw.B, sw.err_scale, sw.err_beta,
+                     out_dtype=torch.bfloat16 if sw.out_bf16 else torch.float32, device=dev)
+    gd = wl.from_u16(g_u16, dev).view(sw.R, sw.N)
+    for _ in range(steps):
+        red.step(gd)
+    torch.cuda.synchronize(dev)
+    out = wl.as_u16(red.out) if sw.out_bf16 else red.out.cpu().numpy()
+    same_out = np.array_equal(np.ascontiguousarray(out).view(np.uint8), want_out.view(np.uint8))
+    same_ef = np.array_equal(red.ef.cpu().numpy().view(np.uint32), want_ef.view(np.uint32))
+    return {"verdict": "bit-exact" if (same_out and same_ef) else "MISMATCH",
+            "shards": bool(same_out), "error_buffers": bool(same_ef),
+            "compared": f"every shard and error-buffer element after {steps} steps of the "
+                        f"CPU baseline's sample (R={sw.R}, N={sw.N}), against the oracle"}
+
+
+def cpu_baseline_qgz(w: wl.QgzWorkload, steps: int, fraction: int, g_full_example=None,
+                     dev=None):
+    """The oracle, as it stands, timed on this host on a bounded sample; with
+    dev, the CUDA path also runs the sample and its result is compared with
+    the oracle's ("parity" entry)."""
     import oracle
     orc = oracle.get()
     sw = qgz_sample(w, fraction)
@@ -771,15 +797,18 @@ def cpu_baseline_qgz(w: wl.QgzWorkload, steps: int, fraction: int, g_full_exampl
     ef = np.zeros(sw.R * sw.N, np.float32)
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle_qgz_step(orc, sw, g, ef)
+        out = oracle_qgz_step(orc, sw, g, ef)
     dt = time.perf_counter() - t0
     cores, model = host_cpu()
-    return {"value": sw.R * sw.N * steps / dt, "unit": "elements/s", "cores": 1,
-            "host_cores": cores, "cpu": model, "kind": "oracle",
-            "sample": f"{steps} steps of R={sw.R} ranks x N={sw.N} elements "
-                      f"(1/{fraction} of each rank's gradient; same B, G, LoCo parameters), "
-                      f"{dt:.1f} s single-threaded",
-            "all_cores": cpu_baseline_qgz_threaded(w, steps, fraction, g)}
+    res = {"value": sw.R * sw.N * steps / dt, "unit": "elements/s", "cores": 1,
+           "host_cores": cores, "cpu": model, "kind": "oracle",
+           "sample": f"{steps} steps of R={sw.R} ranks x N={sw.N} elements "
+                     f"(1/{fraction} of each rank's gradient; same B, G, LoCo parameters), "
+                     f"{dt:.1f} s single-threaded",
+           "all_cores": cpu_baseline_qgz_threaded(w, steps, fraction, g)}
+    if dev is not None:
+        res["parity"] = gpu_parity_on_sample(sw, g, steps, out, ef, dev)
+    return res
 
 
 def run_reference(w_name: str, args, ws, rank):
@@ -881,7 +910,8 @@ def main(argv=None):
             if rank == 0 and ws == 1 and not args.no_cpu_baseline:
                 fraction = {"qgz_tiny": 1, "qgz_single_hop": 4, "qgz_hierarchical": 32}[name]
                 line["cpu_baseline"] = cpu_baseline_qgz(w, 6 if name != "qgz_tiny" else 20,
-                                                        fraction, g_example.cpu())
+                                                        fraction, g_example.cpu(), dev)
+                line["parity"] = line["cpu_baseline"].pop("parity")
             del g_example
         elif name == "qwz":
             qw = wl.QWZ_WEIGHTS
