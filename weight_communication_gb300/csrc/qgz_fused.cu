@@ -121,12 +121,11 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
         const uint32_t x = x0 + 128u * k + 4u * lane;  // destination-major output = slice order
         if (!WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.N)) continue;
         if (OUT_BF16) {
-            const uint32_t h0 = f32_to_bf16_bits(__fmul_rn(acc[k][0], out_scale));
-            const uint32_t h1 = f32_to_bf16_bits(__fmul_rn(acc[k][1], out_scale));
-            const uint32_t h2 = f32_to_bf16_bits(__fmul_rn(acc[k][2], out_scale));
-            const uint32_t h3 = f32_to_bf16_bits(__fmul_rn(acc[k][3], out_scale));
             __stcs(reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + x),
-                   make_uint2(h0 | (h1 << 16), h2 | (h3 << 16)));
+                   make_uint2(f32x2_to_bf16x2_bits(__fmul_rn(acc[k][0], out_scale),
+                                                   __fmul_rn(acc[k][1], out_scale)),
+                              f32x2_to_bf16x2_bits(__fmul_rn(acc[k][2], out_scale),
+                                                   __fmul_rn(acc[k][3], out_scale))));
         } else {
             __stcs(reinterpret_cast<float4 *>(static_cast<float *>(out) + x),
                    make_float4(__fmul_rn(acc[k][0], out_scale), __fmul_rn(acc[k][1], out_scale),

@@ -144,8 +144,7 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
             if (EF == kEfF32) __stcs(reinterpret_cast<float4 *>(ef + x), ev);
             if (EF == kEfBf16)
                 __stcs(reinterpret_cast<uint2 *>(ef16 + x),
-                       make_uint2(uint32_t(f32_to_bf16_bits(ev.x)) | (uint32_t(f32_to_bf16_bits(ev.y)) << 16),
-                                  uint32_t(f32_to_bf16_bits(ev.z)) | (uint32_t(f32_to_bf16_bits(ev.w)) << 16)));
+                       make_uint2(f32x2_to_bf16x2_bits(ev.x, ev.y), f32x2_to_bf16x2_bits(ev.z, ev.w)));
         }
     }
     if ((lane & (LPB - 1)) == 0 && WC_IN_BOUNDS(out0 / B < geo.total / B))

@@ -35,14 +35,14 @@ constexpr uint32_t kOutPerThread = 16;
 template <bool OUT_BF16>
 __device__ __forceinline__ void store16(void *out, uint32_t o, const float acc[16], float out_scale) {
     if (OUT_BF16) {
-        uint32_t h[16];
+        uint32_t h[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) h[j] = f32_to_bf16_bits(__fmul_rn(acc[j], out_scale));
+        for (int j = 0; j < 8; ++j)
+            h[j] = f32x2_to_bf16x2_bits(__fmul_rn(acc[2 * j], out_scale),
+                                        __fmul_rn(acc[2 * j + 1], out_scale));
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
-        __stcs(dst, make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                               h[6] | (h[7] << 16)));
-        __stcs(dst + 1, make_uint4(h[8] | (h[9] << 16), h[10] | (h[11] << 16),
-                                   h[12] | (h[13] << 16), h[14] | (h[15] << 16)));
+        __stcs(dst, make_uint4(h[0], h[1], h[2], h[3]));
+        __stcs(dst + 1, make_uint4(h[4], h[5], h[6], h[7]));
     } else {
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
 #pragma unroll

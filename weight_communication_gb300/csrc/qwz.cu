@@ -9,7 +9,8 @@
 // than the warp tile); lane t holds weights 256*k + 8*t + j, i.e. 16-byte
 // bf16 loads and 8-byte code stores, both fully coalesced.  The raw bf16
 // words stay in registers between the absmax pass and the code pass.
-// Dequantization: one thread per 8 weights, 8-byte code load, 16-byte store.
+// Dequantization: a warp per 1024 weights, 32 per lane from two 16-byte code
+// loads issued together, and 16-byte stores.
 // Codes are rounded and unpacked with exact fp32 arithmetic (wc_device.cuh).
 #include "wc_device.cuh"
 #include "wc_internal.h"
@@ -54,16 +55,17 @@ qwz_quant_int8_kernel(const uint16_t *__restrict__ w, int8_t *__restrict__ codes
         const uint32_t x = tile0 + 256u * k + 8u * lane;
         const uint32_t *h = &raw[k].x;
         uint32_t word[2] = {0u, 0u};
-        uint32_t rep[4] = {0u, 0u, 0u, 0u};
+        float d[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t half = (j & 1) ? (h[j / 2] >> 16) : (h[j / 2] & 0xFFFFu);
             const QCode qc = quant_code<127>(bf16_bits_to_f32(half), bs);
-            const float q = qc.q;
             word[j / 4] |= (qc.bits & 0xFFu) << (8 * (j % 4));
-            if (REPLICA)
-                rep[j / 2] |= uint32_t(f32_to_bf16_bits(dequant(q, bs.scale))) << (16 * (j & 1));
+            d[j] = dequant(qc.q, bs.scale);
         }
+        uint32_t rep[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rep[j] = f32x2_to_bf16x2_bits(d[2 * j], d[2 * j + 1]);
         __stcs(reinterpret_cast<uint2 *>(codes + x), make_uint2(word[0], word[1]));
         if (REPLICA)
             __stcs(reinterpret_cast<uint4 *>(replica + x), make_uint4(rep[0], rep[1], rep[2], rep[3]));
@@ -103,19 +105,17 @@ qwz_dequant_int8_kernel(const int8_t *__restrict__ codes, const float *__restric
         if (!active[k]) continue;
         const uint32_t x = tile0 + 512u * k + 16u * lane;
         const uint32_t qw[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-        uint32_t h[16];
+        uint32_t h[8];
 #pragma unroll
         for (int wq = 0; wq < 4; ++wq) {
             float f[4];
             unpack_int8x4(qw[wq], f);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) h[4 * wq + j] = f32_to_bf16_bits(dequant(f[j], sc[k]));
+            h[2 * wq] = f32x2_to_bf16x2_bits(dequant(f[0], sc[k]), dequant(f[1], sc[k]));
+            h[2 * wq + 1] = f32x2_to_bf16x2_bits(dequant(f[2], sc[k]), dequant(f[3], sc[k]));
         }
         uint4 *dst = reinterpret_cast<uint4 *>(w_out + x);
-        __stcs(dst, make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                               h[6] | (h[7] << 16)));
-        __stcs(dst + 1, make_uint4(h[8] | (h[9] << 16), h[10] | (h[11] << 16),
-                                   h[12] | (h[13] << 16), h[14] | (h[15] << 16)));
+        __stcs(dst, make_uint4(h[0], h[1], h[2], h[3]));
+        __stcs(dst + 1, make_uint4(h[4], h[5], h[6], h[7]));
     }
 }
 

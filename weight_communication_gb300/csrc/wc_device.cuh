@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "wc_internal.h"
 
@@ -75,6 +76,16 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) {
 // fp32 -> bf16 bit pattern, round to nearest even.
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Two fp32 -> two bf16 bit patterns in one word (lo in the low half), each
+// rounded to nearest even: one paired conversion instead of two single ones
+// and the shift and or that join them.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    uint32_t bits;
+    memcpy(&bits, &v, sizeof(bits));  // .x is the low half
+    return bits;
 }
 
 // Max over the `width` lanes of an aligned lane group (width a power of two).
