@@ -21,7 +21,8 @@
 //
 // Fast path (B = 256, 512, 1024 and L a power of two up to 16): one warp per
 // output block, lane t owning outputs t*B/32 .. t*B/32 + B/32 - 1, the source
-// count a template parameter so that all L loads are issued before the adds.
+// count a template parameter so that all L loads are issued before the adds,
+// and a 3-D grid (block, sub-slice, unit) that spares the index divisions.
 // Other shapes: a general kernel (lane groups of 8 consecutive outputs,
 // sources fetched 8 at a time).
 #include "wc_device.cuh"
@@ -146,10 +147,15 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
     constexpr int E = B / kWarp;  // outputs per lane
     constexpr int W = E / 8;      // code words per lane and source
     const int lane = threadIdx.x & (kWarp - 1);
-    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) / kWarp;
-    if (uint64_t(warp) * B >= uint64_t(geo.G) * geo.N) return;  // G*N outputs
-    const uint32_t o = warp * uint32_t(B) + uint32_t(E) * lane;
-    const uint32_t pos0 = hop1_source(geo, o);
+    // Grid x: blocks of one sub-slice (a warp each), y: sub-slice g', z: unit
+    // u = g*L + l -- the positions need no division (L is a power of two).
+    const uint32_t off = (blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp) * B;
+    if (off >= geo.S) return;  // whole warp: the grid's x is rounded up
+    const uint32_t gq = blockIdx.y, u = blockIdx.z;
+    const uint32_t grp = u / L, l = u - grp * L;
+    const uint32_t i = off + uint32_t(E) * lane;
+    const uint32_t o = (u * geo.G + gq) * geo.S + i;  // output element
+    const uint32_t pos0 = grp * L * geo.N + (l * geo.G + gq) * geo.S + i;
     const uint8_t *cp = codes + pos0 / 2;
     const float *sp = scales + pos0 / B;
     const uint32_t cstride = geo.N / 2;
@@ -298,8 +304,8 @@ template <int B, bool HAS_EF>
 static bool launch_fixed_b(const uint8_t *codes, const float *scales, uint8_t *out_codes,
                            float *out_scales, const QgzGeometry &geo, float *ef1, float s,
                            float beta, cudaStream_t stream) {
-    const uint32_t warps = geo.G * geo.N / B;
-    const dim3 grid((warps + 7) / 8);
+    const uint32_t warps = geo.S / B;  // per sub-slice
+    const dim3 grid((warps + 7) / 8, geo.G, geo.R);
     const float omb = 1.0f - beta;
 #define WC_HOP1(LL)                                                                           \
     case LL:                                                                                  \
