@@ -32,14 +32,19 @@ namespace wc {
 constexpr int kMaxFixedSources = 16;
 constexpr uint32_t kOutPerThread = 16;
 
-template <bool OUT_BF16>
-__device__ __forceinline__ void store16(void *out, uint32_t o, const float acc[16], float out_scale) {
+// The 16 sums times out_scale, to fp32 or (rounded to nearest even) bf16.
+// SCALED = false (out_scale == 1) skips the multiplies: x * 1 is exactly x
+// for every float.
+template <bool OUT_BF16, bool SCALED>
+__device__ __forceinline__ void store16(void *out, uint32_t o, const float acc[16],
+                                           float out_scale) {
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = SCALED ? __fmul_rn(acc[j], out_scale) : acc[j];
     if (OUT_BF16) {
         uint32_t h[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            h[j] = f32x2_to_bf16x2_bits(__fmul_rn(acc[2 * j], out_scale),
-                                        __fmul_rn(acc[2 * j + 1], out_scale));
+        for (int j = 0; j < 8; ++j) h[j] = f32x2_to_bf16x2_bits(v[2 * j], v[2 * j + 1]);
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + o);
         __stcs(dst, make_uint4(h[0], h[1], h[2], h[3]));
         __stcs(dst + 1, make_uint4(h[4], h[5], h[6], h[7]));
@@ -47,10 +52,7 @@ __device__ __forceinline__ void store16(void *out, uint32_t o, const float acc[1
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + o);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            __stcs(dst + q, make_float4(__fmul_rn(acc[4 * q], out_scale),
-                                        __fmul_rn(acc[4 * q + 1], out_scale),
-                                        __fmul_rn(acc[4 * q + 2], out_scale),
-                                        __fmul_rn(acc[4 * q + 3], out_scale)));
+            __stcs(dst + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
     }
 }
 
@@ -87,7 +89,7 @@ __device__ __forceinline__ bool output_in_bounds(const QgzGeometry &geo, uint32_
     return uint64_t(k) * geo.S + i + kOutPerThread <= geo.N;
 }
 
-template <int NSRC, bool OUT_BF16>
+template <int NSRC, bool OUT_BF16, bool SCALED>
 __global__ void __launch_bounds__(256)
 dequant_reduce_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                             QgzGeometry geo, uint32_t log2_b, float out_scale,
@@ -119,10 +121,10 @@ dequant_reduce_fixed_kernel(const uint8_t *__restrict__ codes, const float *__re
 #pragma unroll
     for (int t = 0; t < NSRC; ++t) accumulate16(w[t], sc[t], acc);
     if (WC_IN_BOUNDS(output_in_bounds(geo, k, i)))
-        store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
+        store16<OUT_BF16, SCALED>(out, k * geo.S + i, acc, out_scale);
 }
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool SCALED>
 __global__ void __launch_bounds__(256)
 dequant_reduce_loop_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                            QgzGeometry geo, uint32_t nsrc, uint32_t log2_b, float out_scale,
@@ -161,31 +163,32 @@ dequant_reduce_loop_kernel(const uint8_t *__restrict__ codes, const float *__res
             accumulate16(__ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride)),
                          __ldg(sp + size_t(t) * sstride), acc);
     if (WC_IN_BOUNDS(output_in_bounds(geo, k, i)))
-        store16<OUT_BF16>(out, k * geo.S + i, acc, out_scale);
+        store16<OUT_BF16, SCALED>(out, k * geo.S + i, acc, out_scale);
 }
 
-template <int NSRC, bool OUT_BF16>
+template <int NSRC, bool OUT_BF16, bool SCALED>
 static void launch_fixed(const uint8_t *codes, const float *scales, const QgzGeometry &geo,
                          uint32_t log2_b, float out_scale, void *out, dim3 grid,
                          cudaStream_t stream) {
-    dequant_reduce_fixed_kernel<NSRC, OUT_BF16><<<grid, 256, 0, stream>>>(codes, scales, geo,
-                                                                          log2_b, out_scale, out);
+    dequant_reduce_fixed_kernel<NSRC, OUT_BF16, SCALED><<<grid, 256, 0, stream>>>(
+        codes, scales, geo, log2_b, out_scale, out);
 }
 
-template <bool OUT_BF16>
+template <bool OUT_BF16, bool SCALED>
 static void launch_any(const uint8_t *codes, const float *scales, const QgzGeometry &geo,
                        uint32_t nsrc, uint32_t log2_b, float out_scale, void *out, dim3 grid,
                        cudaStream_t stream) {
-#define WC_FIXED(n)                                                                         \
-    case n:                                                                                 \
-        launch_fixed<n, OUT_BF16>(codes, scales, geo, log2_b, out_scale, out, grid, stream); \
+#define WC_FIXED(n)                                                                        \
+    case n:                                                                                \
+        launch_fixed<n, OUT_BF16, SCALED>(codes, scales, geo, log2_b, out_scale, out, grid, \
+                                          stream);                                         \
         return;
     switch (nsrc) {
         WC_FIXED(1) WC_FIXED(2) WC_FIXED(3) WC_FIXED(4) WC_FIXED(5) WC_FIXED(6) WC_FIXED(7)
         WC_FIXED(8) WC_FIXED(9) WC_FIXED(10) WC_FIXED(11) WC_FIXED(12) WC_FIXED(13)
         WC_FIXED(14) WC_FIXED(15) WC_FIXED(16)
         default:
-            dequant_reduce_loop_kernel<OUT_BF16><<<grid, 256, 0, stream>>>(
+            dequant_reduce_loop_kernel<OUT_BF16, SCALED><<<grid, 256, 0, stream>>>(
                 codes, scales, geo, nsrc, log2_b, out_scale, out);
     }
 #undef WC_FIXED
@@ -203,10 +206,16 @@ cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
     const uint32_t threads = 256;
     // S is a multiple of B >= 32, hence of the 16 outputs a thread makes
     const dim3 grid((geo.S / kOutPerThread + threads - 1) / threads, geo.R);
-    if (out_bf16)
-        launch_any<true>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
+    // out_scale == 1 takes the kernels without the final multiplies
+    const bool scaled = out_scale != 1.0f;
+    if (out_bf16 && scaled)
+        launch_any<true, true>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
+    else if (out_bf16)
+        launch_any<true, false>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
+    else if (scaled)
+        launch_any<false, true>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
     else
-        launch_any<false>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
+        launch_any<false, false>(codes, scales, geo, nsrc, log2_b, out_scale, out, grid, stream);
     return cudaPeekAtLastError();
 }
 
