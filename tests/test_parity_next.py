@@ -179,8 +179,7 @@ def test_device_pipeline_matches_serial_steps(dev):
         for t in range(5):
             pipe.step(grads[t])
             snap = torch.empty_like(a.out)
-            pipe.reduce_stream.wait_stream(pipe.reduce_stream)
-            with torch.cuda.stream(pipe.reduce_stream):
+            with torch.cuda.stream(pipe.reduce_stream):  # after step t's reduce
                 snap.copy_(a.out)
             outs.append(snap)
         torch.cuda.synchronize()
