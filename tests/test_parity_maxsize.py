@@ -1,0 +1,175 @@
+"""Parity at the largest sizes the ABI accepts, where 32-bit indexing ends.
+
+qgZ with R*N = 2^32 - 1024 (R = 2), qwZ with n = 2^32 - 2048 and SR with
+n = 2^32 - 1 (its scalar tail included).  The oracle cannot run these sizes
+whole, so sampled blocks at the start and the very end of every rank,
+slice and shard are recomputed on the CPU as small problems of their own.
+For qgZ, one block is one error-feedback quantization problem, and one
+shard block is a reduce of the sources' blocks.  The comparison is bit for
+bit.  About 40 GB of device memory at the peak."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_bits_equal, dev, to_host  # noqa: F401
+from weight_communication_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+ORC = oracle.get()
+
+
+def test_qgz_at_the_largest_size(dev):
+    R, B, s, beta = 2, 256, 1.0, 0.5
+    N = (1 << 31) - 512               # R*N = 2^32 - 1024; B divides N/R
+    S = N // R
+    g = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+    for r in range(R):
+        wl.draw_bf16(N, 1e-3, 7100 + r, dev, out=g[r])
+    gf = g.view(-1)
+    ef = torch.zeros(R * N, dtype=torch.float32, device=dev)
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    out = torch.empty(N, dtype=torch.float32, device=dev)
+    binding.ef_quant_int4(gf, ef, codes, scales, N, R, 1, B, s, beta)
+    binding.dequant_reduce(codes, scales, out, N, R, 1, B)
+    torch.cuda.synchronize()
+    last_block = N // B - 1
+    for r in range(R):
+        for b in (0, S // B - 1, S // B, last_block):       # first/last block of each slice
+            x0 = r * N + b * B
+            e_cpu = np.zeros(B, np.float32)
+            cc, cs = ORC.ef_quant_int4(to_host(gf[x0:x0 + B]).copy(), e_cpu, B, 1, 1, B, s, beta)
+            assert_bits_equal(to_host(codes[x0 // 2:(x0 + B) // 2]), cc, f"codes r={r} b={b}")
+            assert_bits_equal(to_host(scales[x0 // B:x0 // B + 1]), cs, f"scale r={r} b={b}")
+            assert_bits_equal(to_host(ef[x0:x0 + B]), e_cpu, f"error r={r} b={b}")
+    for k in range(R):
+        for j in (0, S // B - 1):
+            # R ranks of R blocks each, whose chunk 0 is block (r, k*S/B + j)
+            mc = np.zeros(R * R * B // 2, np.uint8)
+            ms = np.ones(R * R, np.float32)
+            for r in range(R):
+                src = r * N + k * S + j * B
+                mc[r * R * B // 2:(r * R * B + B) // 2] = to_host(codes[src // 2:(src + B) // 2])
+                ms[r * R] = to_host(scales[src // B:src // B + 1])[0]
+            want = ORC.dequant_reduce(mc, ms, R * B, R, 1, B)[:B]
+            o0 = k * S + j * B
+            assert_bits_equal(to_host(out[o0:o0 + B]), want, f"shard {k} block {j}")
+    del g, ef, codes, scales, out
+    torch.cuda.empty_cache()
+
+
+def test_qwz_at_the_largest_size(dev):
+    B = 2048
+    n = (1 << 32) - B
+    w = wl.draw_bf16(n, 0.02, 7200, dev)
+    codes = torch.empty(n, dtype=torch.int8, device=dev)
+    scales = torch.empty(n // B, dtype=torch.float32, device=dev)
+    back = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    binding.qwz_quant_int8(w, codes, scales, B)
+    binding.qwz_dequant_int8(codes, scales, back, B)
+    torch.cuda.synchronize()
+    for b in (0, n // B // 2, n // B - 1):
+        x0 = b * B
+        oc, os_ = ORC.qwz_quant_int8(to_host(w[x0:x0 + B]).copy(), B)
+        assert_bits_equal(to_host(codes[x0:x0 + B]), oc, f"codes block {b}")
+        assert_bits_equal(to_host(scales[b:b + 1]), os_, f"scale block {b}")
+        assert_bits_equal(to_host(back[x0:x0 + B]), ORC.qwz_dequant_int8(oc, os_, B),
+                          f"dequantized block {b}")
+    del w, codes, scales, back
+    torch.cuda.empty_cache()
+
+
+def test_sr_at_the_largest_size(dev):
+    n = (1 << 32) - 1                 # odd: the last 7 elements take the scalar tail
+    seed, step = 5, 3
+    dst = wl.draw_bf16(n, 1.0, 7300, dev)
+    src = wl.draw_bf16(n, 1e-2, 7301, dev)
+    picks = np.r_[0:16, n // 2:n // 2 + 16, n - 24:n]
+    d0 = to_host(dst[torch.as_tensor(picks, device=dev)]).copy()
+    s0 = to_host(src[torch.as_tensor(picks, device=dev)]).copy()
+    binding.sr_accumulate_bf16(dst, src, seed, step)
+    torch.cuda.synchronize()
+    got = to_host(dst[torch.as_tensor(picks, device=dev)])
+    assert not to_host(src[torch.as_tensor(picks, device=dev)]).any()
+    for j, i in enumerate(picks):
+        x = np.float32(ORC.bf16_to_f32(int(d0[j]))) + np.float32(ORC.bf16_to_f32(int(s0[j])))
+        want = ORC.sr_round(float(x), ORC.sr_bits(seed, step, int(i)))
+        assert int(got[j]) == want, (int(i), int(got[j]), want)
+    del dst, src
+    torch.cuda.empty_cache()
+
+
+def test_small_blocks_at_the_largest_size(dev):
+    """B = 32 takes the kernels' other paths: the tiled EF-quant, the general
+    first hop, qwZ with 8 blocks per warp tile.  Their grid sizes round up
+    from sizes within a tile of 2^32 (a 32-bit rounding would wrap there)."""
+    B = 32
+    # EF-quant (no error buffer) and the one-rank reduce, R*N = 2^32 - 32
+    N = (1 << 32) - B
+    g = wl.draw_bf16(N, 1e-3, 7400, dev)
+    codes = torch.empty(N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(N // B, dtype=torch.float32, device=dev)
+    binding.ef_quant_int4(g, None, codes, scales, N, 1, 1, B, 1.0, 0.0)
+    torch.cuda.synchronize()
+    out = torch.empty(N, dtype=torch.float32, device=dev)
+    binding.dequant_reduce(codes, scales, out, N, 1, 1, B)
+    torch.cuda.synchronize()
+    for b in (0, N // B // 2, N // B - 1):
+        x0 = b * B
+        cc, cs = ORC.ef_quant_int4(to_host(g[x0:x0 + B]).copy(), None, B, 1, 1, B, 1.0, 0.0)
+        assert_bits_equal(to_host(codes[x0 // 2:(x0 + B) // 2]), cc, f"codes block {b}")
+        assert_bits_equal(to_host(scales[b:b + 1]), cs, f"scale block {b}")
+        assert_bits_equal(to_host(out[x0:x0 + B]), ORC.dequant_reduce(cc, cs, B, 1, 1, B),
+                          f"reduced block {b}")
+    del g, codes, scales, out
+    torch.cuda.empty_cache()
+
+    # first hop, general kernel: R = G = 2 (one rank per group), G*N = 2^32 - 128
+    # (B divides the shard N/R)
+    R = G = 2
+    N = (1 << 31) - 2 * B
+    S = N // R
+    g = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+    for r in range(R):
+        wl.draw_bf16(N, 1e-3, 7500 + r, dev, out=g[r])
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    binding.ef_quant_int4(g.view(-1), None, codes, scales, N, R, G, B, 1.0, 0.0)
+    c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    binding.dequant_reduce_requant(codes, scales, c1, s1, N, R, G, B)
+    torch.cuda.synchronize()
+    # unit u (= rank u) sub-slice gq block j requantizes the one source block
+    # at rank u, chunk gq, block j
+    for u in range(R):
+        for gq in range(G):
+            for j in (0, S // B - 1):
+                src = u * N + gq * S + j * B
+                dst = (u * G + gq) * S + j * B
+                mc = to_host(codes[src // 2:(src + B) // 2]).copy()
+                ms = to_host(scales[src // B:src // B + 1]).copy()
+                oc, os_ = ORC.dequant_reduce_requant(mc, ms, B, 1, 1, B)
+                assert_bits_equal(to_host(c1[dst // 2:(dst + B) // 2]), oc, f"hop 1 u={u} gq={gq} j={j}")
+                assert_bits_equal(to_host(s1[dst // B:dst // B + 1]), os_, f"hop 1 scale u={u} gq={gq} j={j}")
+    del g, codes, scales, c1, s1
+    torch.cuda.empty_cache()
+
+    # qwZ with 32-weight blocks, n = 2^32 - 32
+    n = (1 << 32) - B
+    w = wl.draw_bf16(n, 0.02, 7600, dev)
+    qc = torch.empty(n, dtype=torch.int8, device=dev)
+    qs = torch.empty(n // B, dtype=torch.float32, device=dev)
+    back = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    binding.qwz_quant_int8(w, qc, qs, B)
+    binding.qwz_dequant_int8(qc, qs, back, B)
+    torch.cuda.synchronize()
+    for b in (0, n // B - 1):
+        x0 = b * B
+        oc, os_ = ORC.qwz_quant_int8(to_host(w[x0:x0 + B]).copy(), B)
+        assert_bits_equal(to_host(qc[x0:x0 + B]), oc, f"qwZ codes block {b}")
+        assert_bits_equal(to_host(back[x0:x0 + B]), ORC.qwz_dequant_int8(oc, os_, B),
+                          f"qwZ dequantized block {b}")
+    del w, qc, qs, back
+    torch.cuda.empty_cache()

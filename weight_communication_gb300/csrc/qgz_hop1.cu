@@ -332,7 +332,7 @@ static void launch_general_b(const uint8_t *codes, const float *scales, uint8_t 
                              float beta, cudaStream_t stream) {
     constexpr int T = B >= 256 ? B : 256;
     const uint32_t total_out = geo.G * geo.N;
-    const uint32_t tiles = (total_out + T - 1) / T;
+    const uint32_t tiles = uint32_t((uint64_t(total_out) + T - 1) / T);  // no wrap near 2^32
     const uint32_t grid = (tiles + 7) / 8;
     hop1_general_kernel<B, HAS_EF><<<grid, 256, 0, stream>>>(codes, scales, out_codes, out_scales,
                                                              geo, ef1, s, beta, 1.0f - beta);

@@ -164,7 +164,7 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, bool ef_bf16, 
         const uint32_t blocks = geo.S / B;
         grid = dim3((blocks + threads / kWarp - 1) / (threads / kWarp), geo.R, geo.R);
     } else {
-        const uint32_t tiles = (geo.total + T - 1) / T;
+        const uint32_t tiles = uint32_t((uint64_t(geo.total) + T - 1) / T);  // no wrap near 2^32
         grid = dim3((tiles + threads / kWarp - 1) / (threads / kWarp));
     }
     const float omb = 1.0f - beta;

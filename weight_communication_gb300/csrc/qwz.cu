@@ -123,7 +123,7 @@ template <int B>
 static cudaError_t launch_qwz_quant_b(const uint16_t *w, int8_t *codes, float *scales,
                                       uint16_t *replica, uint32_t n, cudaStream_t stream) {
     constexpr int T = B >= 256 ? B : 256;
-    const uint32_t tiles = (n + T - 1) / T;
+    const uint32_t tiles = uint32_t((uint64_t(n) + T - 1) / T);  // no wrap near 2^32
     const uint32_t threads = 256;
     const uint32_t grid = (tiles + threads / kWarp - 1) / (threads / kWarp);
     if (replica)
@@ -155,7 +155,7 @@ cudaError_t launch_qwz_dequant_int8(const int8_t *codes, const float *scales, ui
     uint32_t log2_b = 0;
     while ((1u << log2_b) < uint32_t(B)) ++log2_b;
     const uint32_t threads = 256;
-    const uint32_t warps = (n + 1023) / 1024;
+    const uint32_t warps = uint32_t((uint64_t(n) + 1023) / 1024);  // no wrap near 2^32
     const uint32_t grid = (warps + threads / kWarp - 1) / (threads / kWarp);
     qwz_dequant_int8_kernel<<<grid, threads, 0, stream>>>(codes, scales, w_out, n, log2_b);
     return cudaPeekAtLastError();

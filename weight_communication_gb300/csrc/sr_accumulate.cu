@@ -78,7 +78,7 @@ sr_accumulate_kernel(uint16_t *__restrict__ dst, uint16_t *__restrict__ src, uin
 cudaError_t launch_sr_accumulate(uint16_t *dst, uint16_t *src, uint32_t n, uint32_t seed,
                                  uint32_t step, cudaStream_t stream) {
     const uint32_t threads = 256;
-    const uint32_t nvec = (n + 7) / 8;
+    const uint32_t nvec = uint32_t((uint64_t(n) + 7) / 8);  // n + 7 would wrap at n = 2^32 - 1
     const uint32_t grid = (nvec + threads - 1) / threads;
     sr_accumulate_kernel<<<grid, threads, 0, stream>>>(dst, src, n, sr_key(seed, step));
     return cudaPeekAtLastError();
