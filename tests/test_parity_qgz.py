@@ -123,6 +123,7 @@ REDUCE_CASES = [
     (11, 11 * 64 * 3, 64, True, 1.0 / 11),
     (20, 20 * 128 * 2, 128, False, 1.0),          # more sources than one load batch
     (16, 16 * 1024, 1024, False, 1.0),
+    (1024, 1024 * 32, 32, False, 1.0),            # a thousand sources in the loop kernel
 ]
 
 
@@ -153,6 +154,8 @@ HIER_CASES = [
     (4, 2, 256, 3),        # 2 ranks per group
     (16, 2, 1024, 1),      # 8 ranks per group, 1024-blocks
     (6, 2, 512, 2),        # 3 ranks per group: general kernel at B = 512
+    (64, 32, 32, 1),       # 32 groups: the second hop's source loop (more than 16)
+    (96, 3, 64, 1),        # 32 ranks per group: the general first hop in batches of 8
 ]
 
 
