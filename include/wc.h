@@ -69,7 +69,7 @@ extern "C" {
 
 /*
  * wc_ef_quant_int4 -- error-feedback compensation and int4 quantization of
- * every simulated rank's gradient (LoCo on qgZ; steps a1-a5).
+ * every simulated rank's gradient (LoCo on qgZ).
  *
  * For each rank r in [0, R) and element x of its gradient g_r (N elements):
  *   c = g + s * e                               (fp32; e = ef[r][x])
@@ -116,8 +116,8 @@ WC_API int wc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *ef16,
                                    float err_beta, void *stream);
 
 /*
- * wc_dequant_reduce -- dequantize and reduce in full precision (steps a6-a7,
- * and a9 for the second hop of the hierarchical reduce).
+ * wc_dequant_reduce -- dequantize and reduce in full precision: the flat
+ * reduce after the all-to-all, or the second hop of the hierarchical reduce.
  *
  * Every destination k in [0, R) computes S = N / R outputs
  *   out[k][i] = out_scale * (d_0 + d_1 + ... + d_{n-1})   (fp32, left to right
@@ -142,7 +142,7 @@ WC_API int wc_dequant_reduce(const uint8_t *codes, const float *scales,
 
 /*
  * wc_dequant_reduce_requant -- first (intra-group) hop of the hierarchical
- * reduce, with the partial sums requantized to int4 (step a8).
+ * reduce, with the partial sums requantized to int4.
  *
  * Unit (g, l), local rank l of group g, receives from the L ranks g*L + l'
  * of its group their chunk l (send positions l*G .. l*G+G-1: G sub-slices of
@@ -200,7 +200,7 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes,
                              void *out, int out_dtype, void *stream);
 
 /*
- * wc_qwz_quant_int8 -- qwZ block weight quantization (step a10).
+ * wc_qwz_quant_int8 -- qwZ block weight quantization.
  * Per block of B weights (bf16 widened exactly to fp32), m = max |w|:
  *   m < 127 * 2^-126: scale = 0, q = 0
  *   else: scale = m / 127, inv = 127 / m, q = clamp(rint(w * inv), -127, 127)
@@ -224,7 +224,7 @@ WC_API int wc_qwz_quant_replica_int8(const uint16_t *w, int8_t *codes,
                                      int64_t n, int B, void *stream);
 
 /*
- * wc_qwz_dequant_int8 -- back to bf16 (step a11): w' = bf16_rn(q * scale).
+ * wc_qwz_dequant_int8 -- back to bf16: w' = bf16_rn(q * scale).
  * codes : [n] int8, scales : [n/B] fp32, read.  w_out : [n] bf16, written.
  * Same size rules as wc_qwz_quant_int8.
  */
@@ -233,7 +233,7 @@ WC_API int wc_qwz_dequant_int8(const int8_t *codes, const float *scales,
 
 /*
  * wc_sr_accumulate_bf16 -- ZeRO-2 gradient accumulation with stochastic
- * rounding and the source zeroed in the same kernel (step a12).
+ * rounding and the source zeroed in the same kernel.
  * For i in [0, n):
  *   x = f32(dst[i]) + f32(src[i])                       (fp32)
  *   r = mix(key ^ i) & 0xFFFF,  key = mix(mix(seed) ^ step),

@@ -168,7 +168,7 @@ ORC_EXPORT int64_t orc_send_position(int64_t slice, int R, int G)
 }
 
 /* ------------------------------------------------------------------------ */
-/* a1-a5: error-feedback compensation + int4 quantization, one rank           */
+/* Error-feedback compensation + int4 quantization, one rank                   */
 /* ------------------------------------------------------------------------ */
 
 /*
