@@ -293,6 +293,41 @@ def wire_bytes(w: wl.QgzWorkload) -> dict:
             "exchanges_per_step": 2 if w.G > 1 else 1}
 
 
+def launch_overhead(red, g: torch.Tensor, dev, dist, n: int) -> dict:
+    """The same step issued n times back to back (no flush between steps),
+    once as eager calls and once as replays of a CUDA graph of the step
+    (qgz.GraphedStep): the difference is the host's launch work."""
+    from weight_communication_gb300.qgz import GraphedStep
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    gv = g.reshape(-1)
+    for _ in range(3):
+        red.step(gv)
+    torch.cuda.synchronize(dev)
+    a, b = ev(), ev()
+    a.record()
+    for _ in range(n):
+        red.step(gv)
+    b.record()
+    torch.cuda.synchronize(dev)
+    eager = a.elapsed_time(b) / n
+    graphed = GraphedStep(red)
+    graphed.g.copy_(gv)
+    for _ in range(3):
+        graphed.replay()
+    torch.cuda.synchronize(dev)
+    a, b = ev(), ev()
+    a.record()
+    for _ in range(n):
+        graphed.replay()
+    b.record()
+    torch.cuda.synchronize(dev)
+    graph = a.elapsed_time(b) / n
+    return {"eager_ms_per_step": max_over_ranks(eager, dist, dev),
+            "graph_ms_per_step": max_over_ranks(graph, dist, dev), "steps": n,
+            "how": "steps back to back, no flush: eager binding calls vs one CUDA-graph "
+                   "replay per step (qgz.GraphedStep)"}
+
+
 def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
             hop1_ef: bool = False):
     """One qgZ step per timed iteration; ef_bf16 keeps the error buffer in
@@ -427,6 +462,8 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         "gpu_launches": args.steps * len(names),
         "clocks": clocks,
     }
+    line["launch_overhead"] = launch_overhead(red, batches[0], dev, dist,
+                                              max(1, min(args.steps, 200)))
     if overlapped is not None:
         line["overlapped_ms_per_step"] = overlapped
         line["overlapped_how"] = ("each step's reduce on a second stream beside the next "

@@ -190,3 +190,28 @@ def test_device_pipeline_matches_serial_steps(dev):
         assert torch.equal(a.ef.view(torch.int32), b.ef.view(torch.int32))
         if w.G > 1:
             assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32))
+
+
+def test_graphed_step_matches_eager_steps(dev):
+    """A step captured in a CUDA graph and replayed gives, step after step,
+    the same shards, error buffers and first-hop errors as eager steps."""
+    from weight_communication_gb300.qgz import GraphedStep, QgzReducer
+    for w in (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 16), wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 4)):
+        out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+        a = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                       hop1_ef=w.G > 1)
+        b = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
+                       hop1_ef=w.G > 1)
+        graphed = GraphedStep(a)
+        assert not a.ef.any(), "capturing must not run the step"
+        view = torch.int16 if out_dtype == torch.bfloat16 else torch.int32
+        for t in range(3):
+            g = wl.qgz_gradients(w, t, device=dev)
+            graphed.g.copy_(g.view(-1))
+            got = graphed.replay().clone()
+            want = b.step(g)
+            torch.cuda.synchronize()
+            assert torch.equal(got.view(view), want.view(view)), (w.name, t)
+            assert torch.equal(a.ef.view(torch.int32), b.ef.view(torch.int32)), (w.name, t)
+            if w.G > 1:
+                assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32)), (w.name, t)

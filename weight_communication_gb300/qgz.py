@@ -10,7 +10,10 @@ memory and no extra time.
 
 `QgzReducer` owns the device buffers of one problem (error feedback, send
 buffers, first-hop buffers, reduced shards) and runs a step as 2 launches
-(flat) or 3 launches (hierarchical) on one stream.
+(flat) or 3 launches (hierarchical) on one stream.  `DevicePipeline` overlaps
+each step's reduce with the next quantization, `HostPipeline` runs steps from
+and to host memory with the copies overlapped, and `GraphedStep` replays a
+step captured in a CUDA graph.
 """
 from __future__ import annotations
 
@@ -225,3 +228,36 @@ class HostPipeline:
                 oh.copy_(self.out_dev[b], non_blocking=True)
                 self.out_copied[b].record(self.d2h)
             self._started[b] = True
+
+
+class GraphedStep:
+    """One QgzReducer step captured in a CUDA graph: replay() issues its two
+    or three kernels with a single graph launch, which takes the host's
+    per-call work (argument checks, marshalling, one launch per kernel) off
+    the step.  That matters when the step is short: a small problem is
+    bound by how fast the host can launch, not by the GPU.
+
+    The graph reads its gradient from one fixed device buffer, `g`: copy each
+    step's gradient there (in stream order) before replay().  The error
+    buffers, the send buffers and `red.out` are the reducer's own, so replays
+    advance the error feedback exactly as step() calls do.  The caller keeps
+    the reducer's buffers alive while the graph exists.
+    """
+
+    def __init__(self, red: QgzReducer, stream: torch.cuda.Stream | None = None):
+        self.red = red
+        dev = red.device
+        self.g = torch.zeros(red.R * red.N, dtype=torch.bfloat16, device=dev)
+        self.stream = stream if stream is not None else torch.cuda.Stream(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        self.stream.wait_stream(torch.cuda.current_stream(dev))
+        # the capture records the launches without running them, so the
+        # reducer's state is untouched until the first replay
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            red.step(self.g, self.stream)
+
+    def replay(self) -> torch.Tensor:
+        """Run one step on the contents of self.g; returns red.out (valid in
+        stream order after the replay)."""
+        self.graph.replay()
+        return self.red.out
