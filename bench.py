@@ -946,8 +946,8 @@ def main(argv=None):
             line, g_example = run_qgz(w, args, dev, dist, ws)
             if rank == 0 and ws == 1 and not args.no_cpu_baseline:
                 fraction = {"qgz_tiny": 1, "qgz_single_hop": 4, "qgz_hierarchical": 32}[name]
-                line["cpu_baseline"] = cpu_baseline_qgz(w, 6 if name != "qgz_tiny" else 20,
-                                                        fraction, g_example.cpu(), dev)
+                # about 12 s of single-threaded oracle work on the sample
+                line["cpu_baseline"] = cpu_baseline_qgz(w, 20, fraction, g_example.cpu(), dev)
                 line["parity"] = line["cpu_baseline"].pop("parity")
             del g_example
         elif name == "qwz":
