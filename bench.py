@@ -48,6 +48,10 @@ sys.path.insert(0, str(ROOT))
 from weight_communication_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "qgZ grad elements/s (EF-quant + dequant-reduce) and HBM GB/s vs GB300 peak"
+# --impl reference: total oracle time to aim for, and a conservative
+# single-threaded oracle rate on the host (gradient elements per second)
+REFERENCE_BUDGET_S = 150.0
+ORACLE_ELEMENTS_PER_S = 1.2e8
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 
@@ -857,7 +861,12 @@ def run_reference(w_name: str, args, ws, rank):
     w = wl.QGZ_WORKLOADS.get(w_name)
     if w is None:
         return {"impl": "reference", "unavailable": f"no oracle leg for workload {w_name}"}
+    # Each step is a bounded sample of the workload, sized so that all
+    # warm-up and timed steps take about REFERENCE_BUDGET_S of oracle work
+    # (never more than the fixed fraction below).
     fraction = {"qgz_tiny": 1, "qgz_single_hop": 4, "qgz_hierarchical": 32}[w_name]
+    per_step = REFERENCE_BUDGET_S * ORACLE_ELEMENTS_PER_S / max(1, args.steps + args.warmup)
+    fraction = max(fraction, math.ceil(w.R * w.N / per_step))
     sw = qgz_sample(w, fraction)
     batches = [wl.as_u16(wl.qgz_gradients(sw, t)).ravel().copy() for t in range(2)]
     ef = np.zeros(sw.R * sw.N, np.float32)
