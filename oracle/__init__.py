@@ -74,6 +74,8 @@ _SIGS = {
     "orc_dequant_reduce_requant_ef": (None, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F]),
     "orc_ef_quant_int4_rank_bf16ef": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
     "orc_ef_quant_int4_bf16ef": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_rank_int8ef": (None, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_int8ef": (None, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
     "orc_qwz_quant_replica_int8": (None, [_P, _P, _P, _P, _I64, _I]),
     "orc_qwz_quant_int8": (None, [_P, _P, _P, _I64, _I]),
     "orc_qwz_dequant_int8": (None, [_P, _P, _P, _I64, _I]),
@@ -270,6 +272,20 @@ class Oracle:
         scales = np.zeros(N // B, dtype=np.float32)
         self._lib.orc_ef_quant_int4_rank_bf16ef(_ptr(g_r), _ptr(e16_r), _ptr(codes),
                                                 _ptr(scales), N, R, G, B, s, beta)
+        return codes, scales
+
+    def ef_quant_int4_int8ef(self, g: np.ndarray, e8: np.ndarray, e8s: np.ndarray, N: int,
+                             R: int, G: int, B: int, s: float, beta: float):
+        """All ranks with an int8 error buffer: e8 int8 [R*N] codes and e8s
+        float32 [R*N/B] scales (gradient order), both in place."""
+        _check_qgz(N, R, G, B)
+        assert g.dtype == np.uint16 and g.size == R * N
+        assert e8.dtype == np.int8 and e8.size == R * N
+        assert e8s.dtype == np.float32 and e8s.size == R * N // B
+        codes = np.zeros(R * N // 2, dtype=np.uint8)
+        scales = np.zeros(R * N // B, dtype=np.float32)
+        self._lib.orc_ef_quant_int4_int8ef(_ptr(g), _ptr(e8), _ptr(e8s), _ptr(codes),
+                                           _ptr(scales), N, R, G, B, s, beta)
         return codes, scales
 
     # -- qwZ --------------------------------------------------------------

@@ -299,6 +299,70 @@ ORC_EXPORT void orc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *e16,
                                       N, R, G, B, s, beta);
 }
 
+/*
+ * The same step with an int8 error buffer: a quarter of the fp32 buffer's
+ * memory and traffic ("Merge LoCo with Zero++", Overview: LoCo's cost is the
+ * extra memory of the error buffer).  Reading: the error of each gradient
+ * block (B elements, gradient order) is stored as B int8 codes and one fp32
+ * scale by the block quantizer with qmax = 127 (the qwZ rule: scale = m/127,
+ * codes rint(e * 127/m), zero block below 127 * 2^-126); it is read back as
+ * code * scale, one rounding; every other operation is the binary32 chain of
+ * orc_ef_quant_int4_rank.  e8: N codes and e8s: N/B scales of one rank, in
+ * place (a zero buffer is all-zero codes and scales).
+ */
+ORC_EXPORT void orc_ef_quant_int4_rank_int8ef(const uint16_t *g, int8_t *e8, float *e8s,
+                                              uint8_t *codes, float *scales,
+                                              int64_t N, int R, int G, int B,
+                                              float s, float beta)
+{
+    int64_t S = N / R;
+    float one_mb = 1.0f - beta;
+    float c8[8192];
+    float ev8[8192];
+    float en8[8192];
+    int8_t q8[8192];
+    for (int64_t slice = 0; slice < R; ++slice) {
+        int64_t p = orc_send_position(slice, R, G);
+        for (int64_t b0 = 0; b0 < S; b0 += B) {
+            int64_t in0 = slice * S + b0;
+            int64_t out0 = p * S + b0;
+            float es8 = e8s[in0 / B];
+            for (int i = 0; i < B; ++i) {
+                ev8[i] = orc_dequant(e8[in0 + i], es8);
+                float g8 = orc_bf16_to_f32(g[in0 + i]);
+                float se8 = s * ev8[i];
+                c8[i] = g8 + se8;
+            }
+            float scale;
+            orc_quant_block(c8, B, 7, q8, &scale);
+            scales[out0 / B] = scale;
+            for (int i = 0; i < B; ++i)
+                put_nibble(codes, out0 + i, q8[i]);
+            for (int i = 0; i < B; ++i) {
+                float d8 = orc_dequant(q8[i], scale);
+                float r8 = c8[i] - d8;
+                float k8 = beta * ev8[i];
+                float a8 = one_mb * r8;
+                en8[i] = k8 + a8;
+            }
+            orc_quant_block(en8, B, 127, e8 + in0, &e8s[in0 / B]);
+        }
+    }
+}
+
+ORC_EXPORT void orc_ef_quant_int4_int8ef(const uint16_t *g, int8_t *e8, float *e8s,
+                                         uint8_t *codes, float *scales,
+                                         int64_t N, int R, int G, int B,
+                                         float s, float beta)
+{
+    for (int r = 0; r < R; ++r)
+        orc_ef_quant_int4_rank_int8ef(g + (int64_t)r * N, e8 + (int64_t)r * N,
+                                      e8s + (int64_t)r * (N / B),
+                                      codes + (int64_t)r * (N / 2),
+                                      scales + (int64_t)r * (N / B),
+                                      N, R, G, B, s, beta);
+}
+
 /* ------------------------------------------------------------------------ */
 /* a6-a7 / a9: dequantize and reduce in full precision                        */
 /* ------------------------------------------------------------------------ */

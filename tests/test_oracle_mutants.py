@@ -77,6 +77,11 @@ MUTANTS = {
     "bf16ef_residual_sign": ("float rh = c[i] - dh;", "float rh = dh - c[i];"),
     "nibble_read_unsigned": ("return v >= 8 ? v - 16 : v;", "return v;"),
     "nibble_sign_off_by_one": ("return v >= 8 ? v - 16 : v;", "return v >= 8 ? v - 15 : v;"),
+    "int8ef_stored_with_qmax_7": ("orc_quant_block(en8, B, 127, e8 + in0, &e8s[in0 / B]);",
+                                  "orc_quant_block(en8, B, 7, e8 + in0, &e8s[in0 / B]);"),
+    "int8ef_scale_in_send_order": ("float es8 = e8s[in0 / B];", "float es8 = e8s[out0 / B];"),
+    "int8ef_beta_swapped": ("float k8 = beta * ev8[i];", "float k8 = one_mb * ev8[i];"),
+    "int8ef_compensation_sign": ("c8[i] = g8 + se8;", "c8[i] = g8 - se8;"),
     "sr_step_ignored": ("uint32_t key = orc_mix32(orc_mix32(seed) ^ step);",
                         "uint32_t key = orc_mix32(orc_mix32(seed));"),
 }

@@ -9,6 +9,11 @@
     Overview) -- one step equals the fp32-buffer step with only the stored
     error rounded to bf16 by torch's conversion; over several steps the
     telescoping identity holds up to the bf16 storage rounding;
+  * an int8 error buffer (a quarter of the fp32 buffer's memory) -- a
+    hand-worked two-step example, one step equal to the fp32-buffer step with
+    the stored error quantized by the pinned int8 block rule (in gradient
+    order, also with groups), and the telescoping identity up to the int8
+    storage error;
   * qwZ quantization with the bf16 replica written alongside
     (ZeROPlusPlus.md §1.2) -- equal to quantize then dequantize.
 """
@@ -180,6 +185,87 @@ def test_bf16_error_buffer_telescoping_up_to_storage_rounding(orc):
         slack += np.abs(e_now) * 2.0**-8 + 1e-5 * (np.abs(gt.double().numpy().ravel()) + np.abs(e_now))
     e_T = (e16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     assert np.all(np.abs(sum_d - (sum_g - e_T)) <= slack + 1e-30)
+
+
+# --------------------------------------------------------------------------
+# int8 error buffer
+# --------------------------------------------------------------------------
+
+def _int8_error(e8, e8s, B):
+    """fp64 view of an int8 error buffer: code * scale (exact in fp64)."""
+    return e8.astype(np.float64) * np.repeat(e8s.astype(np.float64), B)
+
+
+def test_int8_error_buffer_worked_example(orc):
+    # B = 32, s = 1, beta = 0.5, one block: g = 7, 3.25, -1.5, 0, ...
+    B = 32
+    g = _bf16([7.0, 3.25, -1.5] + [0.0] * (B - 3))
+    e8 = np.zeros(B, np.int8)
+    e8s = np.zeros(1, np.float32)
+    # step 1 from a zero buffer: m = 7, scale = inv = 1, codes rint(g) with
+    # -1.5 -> -2 (ties to even); c - d = 0, 0.25, 0.5, so the new error is
+    # 0, 0.125, 0.25; stored with m' = 0.25: inv = 127/0.25 = 508 exactly,
+    # codes rint(0, 63.5, 127) = 0, 64 (tie to even), 127
+    codes, scales = orc.ef_quant_int4_int8ef(g, e8, e8s, B, 1, 1, B, 1.0, 0.5)
+    assert unpack_int4(codes)[:4].tolist() == [7, 3, -2, 0] and scales[0] == 1.0
+    assert e8[:4].tolist() == [0, 64, 127, 0] and not e8[4:].any()
+    assert e8s[0] == np.float32(0.25) / np.float32(127)
+    # step 2, same g: the error reads back as about 0, 0.126, 0.25, so
+    # c = 7, 3.376, -1.25 and the codes are 7, 3, -1; the new error
+    # 0.5 e + 0.5 (c - d) is about 0, 0.251 and 0.5 * 0.25 + 0.5 * -0.25 = 0
+    # (to within the rounding of 127 * fl(0.25/127), some 1e-8), stored
+    # against its own maximum 0.251: codes 0, 127, 0
+    codes, scales = orc.ef_quant_int4_int8ef(g, e8, e8s, B, 1, 1, B, 1.0, 0.5)
+    assert unpack_int4(codes)[:4].tolist() == [7, 3, -1, 0]
+    assert e8[:4].tolist() == [0, 127, 0, 0]
+    assert 0.25 < e8s[0] * 127 < 0.252
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_int8_error_buffer_one_step_equals_quantized_fp32(orc, G):
+    """From the same stored error, one step gives the fp32-buffer step's codes
+    and scales, and stores exactly the int8 block quantization (the pinned
+    qwZ rule) of the fp32 step's new error, block by block in gradient order."""
+    R, B = 8, 256
+    w = wl.QgzWorkload(9, "t", R, R * B * 3, G, B, 1.0, 0.5, 1, 1e-3, 1e-3, 100.0, False)
+    g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
+    rng = np.random.default_rng(G)
+    e8 = rng.integers(-127, 128, size=R * w.N).astype(np.int8)
+    e8s = (rng.random(R * w.N // B) * 1e-6).astype(np.float32)
+    e32 = (e8.astype(np.float32) * np.repeat(e8s, B)).astype(np.float32)   # code * scale, one rounding
+    for s, beta in ((1.0, 0.5), (0.5, 0.25)):
+        a8, a8s, a32 = e8.copy(), e8s.copy(), e32.copy()
+        c8, s8 = orc.ef_quant_int4_int8ef(g, a8, a8s, w.N, R, G, B, s, beta)
+        c32, s32 = orc.ef_quant_int4(g, a32, w.N, R, G, B, s, beta)
+        assert np.array_equal(c8, c32) and np.array_equal(s8, s32)
+        for b in range(R * w.N // B):
+            q, sc = orc.quant_block(a32[b * B:(b + 1) * B], 127)
+            assert np.array_equal(a8[b * B:(b + 1) * B], q) and a8s[b] == sc, b
+
+
+def test_int8_error_buffer_telescoping_up_to_storage_error(orc):
+    """Plain error feedback (s = 1, beta = 0): the dequantized values sum to
+    the gradients minus the last stored error, up to the int8 storage error
+    (at most half a storage step per element and step)."""
+    w = wl.QGZ_TINY.scaled(4 * 256 * 64)
+    B = w.B
+    e8 = np.zeros(w.R * w.N, np.int8)
+    e8s = np.zeros(w.R * w.N // B, np.float32)
+    sum_d = np.zeros(w.R * w.N)
+    sum_g = np.zeros(w.R * w.N)
+    slack = np.zeros(w.R * w.N)
+    for t in range(4):
+        gt = wl.qgz_gradients(w, t)
+        g = wl.as_u16(gt).ravel().copy()
+        e_before = _int8_error(e8, e8s, B)
+        codes, scales = orc.ef_quant_int4_int8ef(g, e8, e8s, w.N, w.R, w.G, B, 1.0, 0.0)
+        sum_d += _deq(codes, scales, B)
+        sum_g += gt.double().numpy().ravel()
+        slack += (np.repeat(e8s.astype(np.float64), B) * (0.5 + 2.0**-18)
+                  + 1e-5 * (np.abs(gt.double().numpy().ravel()) + np.abs(e_before)))
+    e_T = _int8_error(e8, e8s, B)
+    assert np.all(np.abs(sum_d - (sum_g - e_T)) <= slack + 1e-30)
+    assert np.any(e8 != 0)
 
 
 # --------------------------------------------------------------------------
