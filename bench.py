@@ -8,11 +8,11 @@ the dequant-reduce of every destination shard.  Metric: gradient elements
 per second (R*N per step) through both kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload qgz_single_hop|qgz_fused|qgz_bf16ef|qgz_hier_ef|
+                    [--workload qgz_single_hop|qgz_fused|qgz_bf16ef|qgz_int8ef|qgz_hier_ef|
                                 qgz_tiny|qgz_hierarchical|qwz|sr|all]
 
 The other workloads: the same step as one fused kernel (qgz_fused), with a
-bf16 error buffer (qgz_bf16ef), the 16-rank two-hop reduce without and with
+bf16 or an int8 error buffer (qgz_bf16ef, qgz_int8ef), the 16-rank two-hop reduce without and with
 first-hop error feedback (qgz_hierarchical, qgz_hier_ef), the L2-resident
 4-rank step (qgz_tiny), the qwZ int8 round trip and one-pass replica (qwz),
 and the bf16 stochastic-rounding accumulate (sr).
@@ -332,15 +332,18 @@ def launch_overhead(red, g: torch.Tensor, dev, dist, n: int) -> dict:
                    "replay per step (qgz.GraphedStep)"}
 
 
-def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
-            hop1_ef: bool = False):
-    """One qgZ step per timed iteration; ef_bf16 keeps the error buffer in
-    bf16 (wc_ef_quant_int4_bf16ef) instead of fp32; hop1_ef adds error
-    feedback to the first hop's requantization (hierarchical only)."""
+EF_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "int8": torch.int8}
+
+
+def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef: str = "fp32", hop1_ef: bool = False):
+    """One qgZ step per timed iteration; ef names the error buffer's form
+    ("fp32", "bf16": wc_ef_quant_int4_bf16ef, "int8": wc_ef_quant_int4_int8ef);
+    hop1_ef adds error feedback to the first hop's requantization
+    (hierarchical only)."""
     from weight_communication_gb300.qgz import QgzReducer
     out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
     red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
-                     ef_dtype=torch.bfloat16 if ef_bf16 else torch.float32, hop1_ef=hop1_ef)
+                     ef_dtype=EF_DTYPES[ef], hop1_ef=hop1_ef)
     g_bytes = w.R * w.N * 2
     nbatch = max(1, min(args.batches, (8 << 30) // g_bytes))
     batches = [wl.qgz_gradients(w, t, device=dev) for t in range(nbatch)]
@@ -419,12 +422,15 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
     # roofline of the dominant kernel (the error-feedback quantization), from
     # its launches inside the timed region
     peak, peak_kind = measured_peaks()
-    ef_bytes = 2 if ef_bf16 else 4
-    efq_bytes = w.R * w.N * (2 + 2 * ef_bytes + 0.5) + w.R * w.N // w.B * 4
+    # error buffer bytes per element, read and written: fp32 4 + 4, bf16 2 + 2,
+    # int8 1 + 1 plus the block scale's share both ways
+    ef_rw = {"fp32": 8.0, "bf16": 4.0, "int8": 2.0 + 8.0 / w.B}[ef]
+    efq_bytes = w.R * w.N * (2 + ef_rw + 0.5) + w.R * w.N // w.B * 4
     efq_ms = per_kernel["ef_quant_int4"]
     achieved = efq_bytes / (efq_ms / 1e3) / 1e9
-    efq_kernel = "ef_quant_int4_bf16ef" if ef_bf16 else "ef_quant_int4"
-    traffic = ncu_traffic(efq_kernel, w.name.split()[0], units) if not ef_bf16 else None
+    efq_kernel = {"fp32": "ef_quant_int4", "bf16": "ef_quant_int4_bf16ef",
+                  "int8": "ef_quant_int4_int8ef"}[ef]
+    traffic = ncu_traffic(efq_kernel, w.name.split()[0], units) if ef == "fp32" else None
     kernels = {}
     S = w.S
     for n in names:
@@ -445,11 +451,11 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef_bf16: bool = False,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded normal gradients with sparse outliers)",
-        "config": {"workload": w.name + (" bf16 error buffer" if ef_bf16 else "")
+        "config": {"workload": w.name + (f" {ef} error buffer" if ef != "fp32" else "")
                    + (" + first-hop error feedback" if hop1_ef else ""),
                    "R": w.R, "N": w.N, "G": w.G, "B": w.B,
                    "err_scale": w.err_scale, "err_beta": w.err_beta,
-                   "ef": "bf16" if ef_bf16 else "fp32",
+                   "ef": ef,
                    "out": "bf16" if w.out_bf16 else "fp32",
                    "l2": ("flushed between steps (untimed 516 MB write)" if flush is not None
                           else f"inputs exceed L2 ({units * 10 / 1e9:.1f} GB per step)"),
@@ -905,8 +911,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
-                    choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_hier_ef", "qgz_tiny",
-                             "qgz_hierarchical", "qwz", "sr", "all"])
+                    choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef",
+                             "qgz_hier_ef", "qgz_tiny", "qgz_hierarchical", "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
@@ -935,16 +941,16 @@ def main(argv=None):
     from weight_communication_gb300 import binding
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
-    names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_tiny", "qgz_hierarchical",
-              "qgz_hier_ef", "qwz",
-              "sr"] if args.workload == "all" else [args.workload])
+    names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef", "qgz_tiny",
+              "qgz_hierarchical", "qgz_hier_ef", "qwz", "sr"]
+             if args.workload == "all" else [args.workload])
     for name in names:
         if name == "qgz_hier_ef":
             w = wl.QGZ_HIERARCHICAL if args.scale == 1 else qgz_sample(wl.QGZ_HIERARCHICAL, args.scale)
             line, _ = run_qgz(w, args, dev, dist, ws, hop1_ef=True)
-        elif name == "qgz_bf16ef":
+        elif name in ("qgz_bf16ef", "qgz_int8ef"):
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
-            line, _ = run_qgz(w, args, dev, dist, ws, ef_bf16=True)
+            line, _ = run_qgz(w, args, dev, dist, ws, ef=name[4:8])
         elif name == "qgz_fused":
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
             line, _ = run_qgz_fused(w, args, dev, dist, ws)

@@ -116,6 +116,27 @@ WC_API int wc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *ef16,
                                    float err_beta, void *stream);
 
 /*
+ * wc_ef_quant_int4_int8ef -- wc_ef_quant_int4 with the error buffer stored in
+ * int8, a quarter of the fp32 buffer's memory ("Merge LoCo with Zero++",
+ * Overview: LoCo's cost is the buffer's extra memory): 4.5 instead of 10.5
+ * bytes per element at B = 256.  The error of each block of B gradient
+ * elements (gradient order) is B int8 codes and one fp32 scale, written by
+ * the block rule of wc_qwz_quant_int8 (scale = m / 127, codes
+ * rint(e * 127 / m), zero block when m < 127 * 2^-126) applied to the new
+ * error, and read back as code * scale (one rounding); all other arithmetic
+ * is the fp32 chain of wc_ef_quant_int4.
+ * ef8        : [R][N] int8 codes, read and written in place (not NULL).
+ * ef8_scales : [R][N/B] fp32, read and written in place (not NULL).
+ * A zero buffer is all-zero codes and scales.  Everything else as
+ * wc_ef_quant_int4.
+ */
+WC_API int wc_ef_quant_int4_int8ef(const uint16_t *g, int8_t *ef8,
+                                   float *ef8_scales, uint8_t *codes,
+                                   float *scales, int64_t N, int R, int G,
+                                   int B, float err_scale, float err_beta,
+                                   void *stream);
+
+/*
  * wc_dequant_reduce -- dequantize and reduce in full precision: the flat
  * reduce after the all-to-all, or the second hop of the hierarchical reduce.
  *

@@ -1,8 +1,9 @@
 """GPU parity (through the C ABI) of the entry points beyond the basic path,
 against the CPU oracle:
 
-  * wc_ef_quant_int4_bf16ef -- EF-quant with a bf16 error buffer, over
-    chained steps, every block size and grouped send orders;
+  * wc_ef_quant_int4_bf16ef and wc_ef_quant_int4_int8ef -- EF-quant with a
+    bf16 or an int8 error buffer, over chained steps, every block size and
+    grouped send orders, and at full size;
   * wc_qwz_quant_replica_int8 -- qwZ quantization writing the bf16 replica.
 
 The fused flat step's parity is in test_parity_qgz.py.
@@ -69,6 +70,54 @@ def test_bf16_error_buffer_full_size(dev):
         assert_bits_equal(to_host(codes), cc, f"codes step {t}")
         assert_bits_equal(to_host(scales), cs, f"scales step {t}")
         assert_bits_equal(to_host(e_dev), e_cpu, f"bf16 error step {t}")
+
+
+@pytest.mark.parametrize("R,N,G,B,s,beta", BF16EF_CASES)
+def test_int8_error_buffer_parity(dev, R, N, G, B, s, beta):
+    """int8 error buffer over three chained steps, from random stored codes and
+    scales: codes, scales, stored error codes and error scales bit for bit."""
+    rng = np.random.default_rng(N + 3 * B)
+    e8_0 = rng.integers(-127, 128, size=R * N).astype(np.int8)
+    es_0 = (rng.random(R * N // B) * 1e-5).astype(np.float32)
+    es_0[::7] = 0.0                                   # some zero blocks in the buffer
+    e8_cpu, es_cpu = e8_0.copy(), es_0.copy()
+    e8_dev, es_dev = to_dev(e8_0, dev), to_dev(es_0, dev)
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    for t in range(3):
+        g = edge_gradients(R, N, B, seed=17 * t + R + B)
+        binding.ef_quant_int4_int8ef(to_dev(g, dev), e8_dev, es_dev, codes, scales, N, R, G, B,
+                                     s, beta)
+        torch.cuda.synchronize()
+        cc, cs = ORC.ef_quant_int4_int8ef(g, e8_cpu, es_cpu, N, R, G, B, s, beta)
+        assert_bits_equal(to_host(codes), cc, f"codes step {t}")
+        assert_bits_equal(to_host(scales), cs, f"scales step {t}")
+        assert_bits_equal(to_host(e8_dev), e8_cpu, f"int8 error codes step {t}")
+        assert_bits_equal(to_host(es_dev), es_cpu, f"int8 error scales step {t}")
+
+
+def test_int8_error_buffer_full_size(dev):
+    """Single-hop workload size, two chained steps from a zero buffer, every
+    output."""
+    w = wl.QGZ_SINGLE_HOP
+    e8_dev = torch.zeros(w.R * w.N, dtype=torch.int8, device=dev)
+    es_dev = torch.zeros(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+    e8_cpu = np.zeros(w.R * w.N, np.int8)
+    es_cpu = np.zeros(w.R * w.N // w.B, np.float32)
+    codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+    gd = torch.empty((w.R, w.N), dtype=torch.bfloat16, device=dev)
+    for t in range(2):
+        wl.qgz_gradients(w, t, device=dev, out=gd)
+        binding.ef_quant_int4_int8ef(gd.view(-1), e8_dev, es_dev, codes, scales, w.N, w.R, 1, w.B,
+                                     w.err_scale, w.err_beta)
+        torch.cuda.synchronize()
+        cc, cs = ORC.ef_quant_int4_int8ef(to_host(gd).ravel(), e8_cpu, es_cpu, w.N, w.R, 1, w.B,
+                                          w.err_scale, w.err_beta)
+        assert_bits_equal(to_host(codes), cc, f"codes step {t}")
+        assert_bits_equal(to_host(scales), cs, f"scales step {t}")
+        assert_bits_equal(to_host(e8_dev), e8_cpu, f"int8 error codes step {t}")
+        assert_bits_equal(to_host(es_dev), es_cpu, f"int8 error scales step {t}")
 
 
 HOP1_EF_CASES = [

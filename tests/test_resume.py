@@ -1,7 +1,8 @@
-"""Checkpoint and resume: the error buffers are the only state a qgZ step
-carries from one step to the next (LoCo's extra memory, "Merge LoCo with
-Zero++", Overview).  Saving them after step k, loading them into a fresh
-reducer and continuing must reproduce an uninterrupted run bit for bit."""
+"""Checkpoint and resume: the error buffers (with the int8 buffer's scales)
+are the only state a qgZ step carries from one step to the next (LoCo's
+extra memory, "Merge LoCo with Zero++", Overview).  Saving them after step k,
+loading them into a fresh reducer and continuing must reproduce an
+uninterrupted run bit for bit."""
 import pytest
 import torch
 
@@ -20,6 +21,7 @@ def _reducer(w, dev, ef_dtype):
 
 @pytest.mark.parametrize("name,ef_dtype", [("single_hop", torch.float32),
                                            ("single_hop", torch.bfloat16),
+                                           ("single_hop", torch.int8),
                                            ("hierarchical", torch.float32)])
 def test_resume_from_saved_error_buffers(dev, tmp_path, name, ef_dtype):
     w = (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 32) if name == "single_hop"
@@ -34,19 +36,25 @@ def test_resume_from_saved_error_buffers(dev, tmp_path, name, ef_dtype):
     for g in grads[:k]:
         first.step(g)
     ckpt = tmp_path / "qgz_state.pt"
-    torch.save({"ef": first.ef.cpu(), "ef1": None if first.ef1 is None else first.ef1.cpu()}, ckpt)
+    torch.save({"ef": first.ef.cpu(),
+                "ef_scales": None if first.ef_scales is None else first.ef_scales.cpu(),
+                "ef1": None if first.ef1 is None else first.ef1.cpu()}, ckpt)
     del first
 
     state = torch.load(ckpt)
     resumed = _reducer(w, dev, ef_dtype)
     resumed.ef.copy_(state["ef"])
+    if state["ef_scales"] is not None:
+        resumed.ef_scales.copy_(state["ef_scales"])
     if state["ef1"] is not None:
         resumed.ef1.copy_(state["ef1"])
     for t in range(k, steps):
         out = resumed.step(grads[t])
         assert torch.equal(out.view(torch.int16 if w.out_bf16 else torch.int32),
                            ref[t].view(torch.int16 if w.out_bf16 else torch.int32)), t
-    assert torch.equal(resumed.ef.view(torch.int16 if ef_dtype == torch.bfloat16 else torch.int32),
-                       whole.ef.view(torch.int16 if ef_dtype == torch.bfloat16 else torch.int32))
+    bits = {torch.float32: torch.int32, torch.bfloat16: torch.int16, torch.int8: torch.int8}[ef_dtype]
+    assert torch.equal(resumed.ef.view(bits), whole.ef.view(bits))
+    if whole.ef_scales is not None:
+        assert torch.equal(resumed.ef_scales.view(torch.int32), whole.ef_scales.view(torch.int32))
     if whole.ef1 is not None:
         assert torch.equal(resumed.ef1.view(torch.int32), whole.ef1.view(torch.int32))

@@ -33,6 +33,7 @@ SIGNATURES = {
     "wc_dequant_reduce_requant_ef": [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F, _P],
     "wc_qgz_step_fused": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
     "wc_ef_quant_int4_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
+    "wc_ef_quant_int4_int8ef": [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
     "wc_qwz_quant_replica_int8": [_P, _P, _P, _P, _I64, _I, _P],
     "wc_qwz_dequant_int8": [_P, _P, _P, _I64, _I, _P],
@@ -224,6 +225,20 @@ def ef_quant_int4_bf16ef(g: torch.Tensor, ef16: torch.Tensor, codes: torch.Tenso
     d = g.device
     _call(d, "wc_ef_quant_int4_bf16ef", _dev(g, "g", torch.bfloat16, R * N, d),
           _dev(ef16, "ef16", torch.bfloat16, R * N, d),
+          _dev(codes, "codes", torch.uint8, R * N // 2, d),
+          _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
+          _stream(g, stream))
+
+
+def ef_quant_int4_int8ef(g: torch.Tensor, ef8: torch.Tensor, ef8_scales: torch.Tensor,
+                         codes: torch.Tensor, scales: torch.Tensor, N: int, R: int, G: int, B: int,
+                         err_scale: float = 1.0, err_beta: float = 0.0, stream=None) -> None:
+    """wc_ef_quant_int4_int8ef: as ef_quant_int4 with an int8 error buffer
+    (ef8 int8 [R*N] codes, ef8_scales fp32 [R*N/B], both in place)."""
+    d = g.device
+    _call(d, "wc_ef_quant_int4_int8ef", _dev(g, "g", torch.bfloat16, R * N, d),
+          _dev(ef8, "ef8", torch.int8, R * N, d),
+          _dev(ef8_scales, "ef8_scales", torch.float32, R * N // B, d),
           _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
           _stream(g, stream))

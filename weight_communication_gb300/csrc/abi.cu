@@ -81,8 +81,9 @@ WC_API int wc_ef_quant_int4(const uint16_t *g, float *ef, uint8_t *codes, float 
     WC_REQUIRE_PTR(fn, codes);
     WC_REQUIRE_PTR(fn, scales);
     if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
-    return from_cuda(wc::launch_ef_quant_int4(g, ef, false, codes, scales, geo, B, err_scale,
-                                              err_beta, static_cast<cudaStream_t>(stream)),
+    return from_cuda(wc::launch_ef_quant_int4(g, ef, wc::kEfModeF32, nullptr, codes, scales, geo,
+                                              B, err_scale, err_beta,
+                                              static_cast<cudaStream_t>(stream)),
                      fn);
 }
 
@@ -98,8 +99,28 @@ WC_API int wc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *ef16, uint8_t *c
     WC_REQUIRE_PTR(fn, ef16);
     WC_REQUIRE_PTR(fn, codes);
     WC_REQUIRE_PTR(fn, scales);
-    return from_cuda(wc::launch_ef_quant_int4(g, ef16, true, codes, scales, geo, B, err_scale,
-                                              err_beta, static_cast<cudaStream_t>(stream)),
+    return from_cuda(wc::launch_ef_quant_int4(g, ef16, wc::kEfModeBf16, nullptr, codes, scales,
+                                              geo, B, err_scale, err_beta,
+                                              static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
+WC_API int wc_ef_quant_int4_int8ef(const uint16_t *g, int8_t *ef8, float *ef8_scales,
+                                   uint8_t *codes, float *scales, int64_t N, int R, int G,
+                                   int B, float err_scale, float err_beta, void *stream) {
+    static const char *fn = "wc_ef_quant_int4_int8ef";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, g);
+    WC_REQUIRE_PTR(fn, ef8);
+    WC_REQUIRE_PTR(fn, ef8_scales);
+    WC_REQUIRE_PTR(fn, codes);
+    WC_REQUIRE_PTR(fn, scales);
+    return from_cuda(wc::launch_ef_quant_int4(g, ef8, wc::kEfModeInt8, ef8_scales, codes, scales,
+                                              geo, B, err_scale, err_beta,
+                                              static_cast<cudaStream_t>(stream)),
                      fn);
 }
 

@@ -31,24 +31,30 @@ namespace wc {
 // then fully coalesced: 8-byte bf16 loads (256 B per warp instruction),
 // 16-byte fp32 error loads and stores (512 B), 2-byte code stores (64 B).
 //
-// EF selects the error buffer: none, fp32 (4 bytes per element each way) or
-// bf16 (2 bytes; the new error is rounded to the nearest bf16 when stored).
-enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2 };
+// EF selects the error buffer: none, fp32 (4 bytes per element each way),
+// bf16 (2 bytes; the new error is rounded to the nearest bf16 when stored) or
+// int8 (1 byte, plus one fp32 scale per block: the new error of a block is
+// quantized by the int8 absmax rule once the whole block is known, so it is
+// kept in registers until a second shuffle reduction has found its maximum).
+enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2, kEfInt8 = 3 };
 
 template <int B, int EF>
 __global__ void __launch_bounds__(256)
 ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
-                     uint8_t *__restrict__ codes, float *__restrict__ scales,
-                     QgzGeometry geo, float s, float beta, float one_minus_beta) {
+                     float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
+                     float *__restrict__ scales, QgzGeometry geo, float s, float beta,
+                     float one_minus_beta) {
     constexpr bool HAS_EF = EF != kEfNone;
     float *__restrict__ ef = static_cast<float *>(ef_v);
     uint16_t *__restrict__ ef16 = static_cast<uint16_t *>(ef_v);
+    int8_t *__restrict__ ef8 = static_cast<int8_t *>(ef_v);
     constexpr int T = B >= 128 ? B : 128;
     constexpr int K = T / 128;
     constexpr int LPB = B >= 128 ? 32 : B / 4;  // lanes per block
     const int lane = threadIdx.x & (kWarp - 1);
     uint32_t tile0;  // first gradient element of the warp's tile
     uint32_t out0;   // code position of the first element of the lane's block
+    uint32_t eblk;   // the lane's block in gradient order (int8 error scales)
     bool active;
     if (B >= 128) {
         // Grid x: blocks of one slice (a warp each), y: slice, z: rank -- the
@@ -63,6 +69,7 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         }
         tile0 = r * geo.N + slice * geo.S + off;
         out0 = r * geo.N + p * geo.S + off;
+        eblk = tile0 / B;
         active = true;
     } else {
         // 1-D grid of 128-element tiles holding 128/B blocks each.
@@ -74,6 +81,7 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         const uint32_t first = tile0 + 4u * lane;
         active = first < geo.total;
         const uint32_t blk = first / B;
+        eblk = blk;
         const uint32_t r = blk / geo.blocks_per_rank;
         const uint32_t x0 = (blk - r * geo.blocks_per_rank) * B;  // element in rank
         const uint32_t slice = x0 / geo.S;
@@ -85,6 +93,8 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
 
     float c[K][4];
     float e[K][4];
+    float es = 0.0f;  // int8 error: the block's stored scale
+    if (EF == kEfInt8 && active && WC_IN_BOUNDS(eblk < geo.total / B)) es = __ldg(ef_scales + eblk);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         const uint32_t x = tile0 + 128u * k + 4u * lane;
@@ -97,6 +107,12 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                 const uint2 eh = ld_stream_u2(ef16 + x);
                 ev = make_float4(bf16_bits_to_f32(eh.x & 0xFFFFu), bf16_bits_to_f32(eh.x >> 16),
                                  bf16_bits_to_f32(eh.y & 0xFFFFu), bf16_bits_to_f32(eh.y >> 16));
+            }
+            if (EF == kEfInt8) {
+                float f[4];
+                unpack_int8x4(__ldcs(reinterpret_cast<const unsigned int *>(ef8 + x)), f);
+                ev = make_float4(dequant(f[0], es), dequant(f[1], es), dequant(f[2], es),
+                                 dequant(f[3], es));
             }
         }
         const float gf[4] = {bf16_bits_to_f32(gv.x & 0xFFFFu), bf16_bits_to_f32(gv.x >> 16),
@@ -114,7 +130,9 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         for (int j = 0; j < 4; ++j) m = fmaxf(m, fabsf(c[k][j]));
     m = group_max<LPB>(m);
     const BlockScale bs = block_scale<7>(m);
-    if (!active) return;
+    // int8 error: every lane takes part in the second reduction below
+    if (EF != kEfInt8 && !active) return;
+    float en[EF == kEfInt8 ? K : 1][4];  // int8 error: the new error, until stored
 
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -128,7 +146,7 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
         }
         const uint32_t in_blk = B >= 128 ? 128u * k + 4u * lane : (4u * lane) % B;
         const uint32_t pos = out0 + in_blk;
-        if (WC_IN_BOUNDS(uint64_t(pos) + 4 <= geo.total))
+        if (active && WC_IN_BOUNDS(uint64_t(pos) + 4 <= geo.total))
             __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2), (unsigned short)packed);
         if (HAS_EF) {
             float4 ev;
@@ -139,6 +157,11 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                 o[j] = __fadd_rn(__fmul_rn(beta, e[k][j]),
                                  __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));
             }
+            if (EF == kEfInt8) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) en[EF == kEfInt8 ? k : 0][j] = o[j];
+                continue;
+            }
             const uint32_t x = tile0 + 128u * k + 4u * lane;
             if (!WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) continue;
             if (EF == kEfF32) __stcs(reinterpret_cast<float4 *>(ef + x), ev);
@@ -147,14 +170,38 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                        make_uint2(f32x2_to_bf16x2_bits(ev.x, ev.y), f32x2_to_bf16x2_bits(ev.z, ev.w)));
         }
     }
-    if ((lane & (LPB - 1)) == 0 && WC_IN_BOUNDS(out0 / B < geo.total / B))
+    if (active && (lane & (LPB - 1)) == 0 && WC_IN_BOUNDS(out0 / B < geo.total / B))
         __stcs(scales + out0 / B, bs.scale);
+
+    if (EF == kEfInt8) {
+        // the new error of the block, quantized by the int8 absmax rule
+        float m8 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m8 = fmaxf(m8, fabsf(en[EF == kEfInt8 ? k : 0][j]));
+        m8 = group_max<LPB>(m8);
+        const BlockScale bse = block_scale<127>(m8);
+        if (!active) return;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                word |= (quant_code<127>(en[EF == kEfInt8 ? k : 0][j], bse).bits & 0xFFu) << (8 * j);
+            const uint32_t x = tile0 + 128u * k + 4u * lane;
+            if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total))
+                __stcs(reinterpret_cast<unsigned int *>(ef8 + x), word);
+        }
+        if ((lane & (LPB - 1)) == 0 && WC_IN_BOUNDS(eblk < geo.total / B))
+            __stcs(ef_scales + eblk, bse.scale);
+    }
 }
 
 template <int B>
-static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
-                                     float *scales, const QgzGeometry &geo, float s,
-                                     float beta, cudaStream_t stream) {
+static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, float *ef_scales,
+                                     uint8_t *codes, float *scales, const QgzGeometry &geo,
+                                     float s, float beta, cudaStream_t stream) {
     constexpr int T = B >= 128 ? B : 128;
     const uint32_t threads = 256;
     dim3 grid;
@@ -168,32 +215,31 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, bool ef_bf16, 
         grid = dim3((tiles + threads / kWarp - 1) / (threads / kWarp));
     }
     const float omb = 1.0f - beta;
-    if (ef == nullptr)
-        ef_quant_int4_kernel<B, kEfNone><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
-                                                                        s, beta, omb);
-    else if (ef_bf16)
-        ef_quant_int4_kernel<B, kEfBf16><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
-                                                                        s, beta, omb);
-    else
-        ef_quant_int4_kernel<B, kEfF32><<<grid, threads, 0, stream>>>(g, ef, codes, scales, geo,
-                                                                       s, beta, omb);
+#define WC_EFQ(MODE)                                                                       \
+    ef_quant_int4_kernel<B, MODE><<<grid, threads, 0, stream>>>(g, ef, ef_scales, codes,    \
+                                                               scales, geo, s, beta, omb)
+    if (ef == nullptr) WC_EFQ(kEfNone);
+    else if (ef_mode == kEfBf16) WC_EFQ(kEfBf16);
+    else if (ef_mode == kEfInt8) WC_EFQ(kEfInt8);
+    else WC_EFQ(kEfF32);
+#undef WC_EFQ
     return cudaPeekAtLastError();
 }
 
 WC_CHECK_RECORD_READER(check_record_qgz_quant)
 
-cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
-                                 float *scales, const QgzGeometry &geo, int B, float s,
-                                 float beta, cudaStream_t stream) {
+cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, int ef_mode, float *ef_scales,
+                                 uint8_t *codes, float *scales, const QgzGeometry &geo, int B,
+                                 float s, float beta, cudaStream_t stream) {
+#define WC_EFQ_B(BB)                                                                       \
+    case BB:                                                                               \
+        return launch_ef_quant_b<BB>(g, ef, ef_mode, ef_scales, codes, scales, geo, s, beta, \
+                                     stream);
     switch (B) {
-        case 32: return launch_ef_quant_b<32>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
-        case 64: return launch_ef_quant_b<64>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
-        case 128: return launch_ef_quant_b<128>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
-        case 256: return launch_ef_quant_b<256>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
-        case 512: return launch_ef_quant_b<512>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
-        case 1024: return launch_ef_quant_b<1024>(g, ef, ef_bf16, codes, scales, geo, s, beta, stream);
+        WC_EFQ_B(32) WC_EFQ_B(64) WC_EFQ_B(128) WC_EFQ_B(256) WC_EFQ_B(512) WC_EFQ_B(1024)
         default: return cudaErrorInvalidValue;
     }
+#undef WC_EFQ_B
 }
 
 }  // namespace wc

@@ -19,10 +19,12 @@ struct QgzGeometry {
     uint32_t total;            // R * N
 };
 
-// ef: fp32 [R][N], bf16 [R][N] (ef_bf16) or NULL.
-cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, bool ef_bf16, uint8_t *codes,
-                                 float *scales, const QgzGeometry &geo, int B, float s,
-                                 float beta, cudaStream_t stream);
+// ef: NULL, or the error buffer [R][N] in the form ef_mode names: 1 fp32,
+// 2 bf16, 3 int8 codes with ef_scales [R][N/B] fp32 (gradient order).
+constexpr int kEfModeF32 = 1, kEfModeBf16 = 2, kEfModeInt8 = 3;
+cudaError_t launch_ef_quant_int4(const uint16_t *g, void *ef, int ef_mode, float *ef_scales,
+                                 uint8_t *codes, float *scales, const QgzGeometry &geo, int B,
+                                 float s, float beta, cudaStream_t stream);
 cudaError_t launch_dequant_reduce(const uint8_t *codes, const float *scales,
                                   const QgzGeometry &geo, int B, float out_scale, void *out,
                                   bool out_bf16, cudaStream_t stream);

@@ -25,7 +25,8 @@ from . import binding
 class QgzReducer:
     """Device state and launches of one (R, N, G, B) quantized reduce.
 
-    error feedback : fp32 [R, N], persistent across steps (zeroed at start)
+    error feedback : fp32 or bf16 [R, N], or int8 [R, N] with fp32 scales
+                     [R, N/B]; persistent across steps (zeroed at start)
     codes, scales  : int4 send buffers [R, N/2] bytes and [R, N/B] fp32
     hop1 codes/sc. : first-hop outputs [G*N/2], [G*N/B] (G > 1 only)
     out            : reduced shards [N] (= [R][S]), fp32 or bf16
@@ -35,8 +36,10 @@ class QgzReducer:
                  err_beta: float = 0.0, use_ef: bool = True, out_dtype=torch.float32,
                  out_scale: float = 1.0, device="cuda", ef_dtype=torch.float32,
                  hop1_ef: bool = False):
-        """ef_dtype: torch.float32, or torch.bfloat16 for the half-size error
-        buffer (wc_ef_quant_int4_bf16ef).  hop1_ef (G > 1): keep an fp32 error
+        """ef_dtype: torch.float32, torch.bfloat16 for the half-size error
+        buffer (wc_ef_quant_int4_bf16ef), or torch.int8 for the quarter-size
+        one (wc_ef_quant_int4_int8ef: int8 codes in self.ef, one fp32 scale per
+        block in self.ef_scales).  hop1_ef (G > 1): keep an fp32 error
         for the first hop's requantization too (wc_dequant_reduce_requant_ef),
         with the same err_scale and err_beta."""
         self.N, self.R, self.G, self.B = N, R, G, B
@@ -44,9 +47,11 @@ class QgzReducer:
         self.out_scale = out_scale
         self.device = torch.device(device)
         dev = self.device
-        if ef_dtype not in (torch.float32, torch.bfloat16):
-            raise TypeError("ef_dtype must be float32 or bfloat16")
+        if ef_dtype not in (torch.float32, torch.bfloat16, torch.int8):
+            raise TypeError("ef_dtype must be float32, bfloat16 or int8")
         self.ef = torch.zeros(R * N, dtype=ef_dtype, device=dev) if use_ef else None
+        self.ef_scales = (torch.zeros(R * N // B, dtype=torch.float32, device=dev)
+                          if use_ef and ef_dtype == torch.int8 else None)
         self.codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
         self.scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
         if G > 1:
@@ -69,6 +74,10 @@ class QgzReducer:
             binding.ef_quant_int4_bf16ef(g.reshape(-1), self.ef, codes, scales, self.N,
                                          self.R, self.G, self.B, self.err_scale, self.err_beta,
                                          stream)
+        elif self.ef is not None and self.ef.dtype == torch.int8:
+            binding.ef_quant_int4_int8ef(g.reshape(-1), self.ef, self.ef_scales, codes, scales,
+                                         self.N, self.R, self.G, self.B, self.err_scale,
+                                         self.err_beta, stream)
         else:
             binding.ef_quant_int4(g.reshape(-1), self.ef, codes, scales, self.N, self.R,
                                   self.G, self.B, self.err_scale, self.err_beta, stream)
