@@ -168,3 +168,89 @@ def test_random_geometry_fused_step(dev, seed):
         assert_bits_equal(to_host(out), want, f"shards, step {t}")
         if ef is not None:
             assert_bits_equal(to_host(ef), orc.e, f"error buffer, step {t}")
+
+
+QWZ_SEEDS = list(range(40))
+
+
+def draw_qwz(seed: int) -> dict:
+    rng = np.random.default_rng(7_000_003 * seed + 5)
+    B = 32 << int(rng.integers(0, 8))
+    blocks = (int(rng.integers(1, 41)) if rng.integers(0, 2)
+              else int(rng.integers(1, max(2, (1 << 20) // B))))
+    return dict(B=B, n=B * blocks,
+                sigma=float(rng.choice([1e-6, 1e-3, 0.02, 3.0])),
+                replica=bool(rng.integers(0, 2)), zero_blocks=bool(rng.integers(0, 2)))
+
+
+@pytest.mark.parametrize("seed", QWZ_SEEDS,
+                         ids=[f"s{s}-B{draw_qwz(s)['B']}-n{draw_qwz(s)['n']}" for s in QWZ_SEEDS])
+def test_random_qwz(dev, seed):
+    """qwZ int8 block quantization (with or without the bf16 replica) and its
+    dequantization for a random block size in [32, 4096] and block count
+    ("ZeRO++", qwZ)."""
+    q = draw_qwz(seed)
+    n, B = q["n"], q["B"]
+    w = wl.as_u16(wl.draw_bf16(n, q["sigma"], 104729 * seed + 1, outlier_frac=1e-3,
+                               outlier_mult=30.0)).copy()
+    if q["zero_blocks"]:
+        for b in np.random.default_rng(seed).choice(n // B, size=min(n // B, 2), replace=False):
+            w[b * B:(b + 1) * B] = 0
+    codes = torch.empty(n, dtype=torch.int8, device=dev)
+    scales = torch.empty(n // B, dtype=torch.float32, device=dev)
+    back = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    if q["replica"]:
+        rep = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        binding.qwz_quant_replica_int8(to_dev(w, dev), codes, scales, rep, B)
+        oc, os_, orep = ORC.qwz_quant_replica_int8(w, B)
+    else:
+        binding.qwz_quant_int8(to_dev(w, dev), codes, scales, B)
+        oc, os_ = ORC.qwz_quant_int8(w, B)
+    binding.qwz_dequant_int8(codes, scales, back, B)
+    torch.cuda.synchronize()
+    assert_bits_equal(to_host(codes), oc, "int8 codes")
+    assert_bits_equal(to_host(scales), os_, "scales")
+    if q["replica"]:
+        assert_bits_equal(to_host(rep), orep, "bf16 replica")
+    assert_bits_equal(to_host(back), ORC.qwz_dequant_int8(oc, os_, B), "dequantized bf16")
+
+
+SR_SEEDS = list(range(40))
+
+
+def draw_sr(seed: int) -> dict:
+    rng = np.random.default_rng(9_000_011 * seed + 3)
+    n = int(rng.integers(1, 64)) if rng.integers(0, 4) == 0 else int(rng.integers(1, 1 << 19))
+    return dict(n=n, offset=int(rng.integers(0, 8)) * 8,
+                seed=int(rng.integers(0, 1 << 32)), step0=int(rng.integers(0, 1 << 32)),
+                ratio=float(rng.choice([1.0, 1e-2, 1e-4, 1e-8])))
+
+
+@pytest.mark.parametrize("seed", SR_SEEDS,
+                         ids=[f"s{s}-n{draw_sr(s)['n']}" for s in SR_SEEDS])
+def test_random_sr_accumulate(dev, seed):
+    """bf16 stochastic-rounding accumulate of a random length, starting at a
+    random 16-byte-aligned offset into its buffers, with random seed and step
+    counters and a random source-to-destination magnitude ratio, over three
+    micro-steps ("Stochastic rounding", vector_add)."""
+    p = draw_sr(seed)
+    n, off = p["n"], p["offset"]
+    rng = np.random.default_rng(seed)
+
+    def bf16(x):
+        return wl.as_u16(torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)).copy()
+
+    dst = bf16(rng.standard_normal(n))
+    dbuf = torch.zeros(n + off, dtype=torch.bfloat16, device=dev)
+    sbuf = torch.zeros(n + off, dtype=torch.bfloat16, device=dev)
+    dbuf[off:].copy_(to_dev(dst, dev))
+    for t in range(3):
+        step = (p["step0"] + t) & 0xFFFFFFFF
+        src = bf16(rng.standard_normal(n) * p["ratio"])
+        sbuf[off:].copy_(to_dev(src, dev))
+        binding.sr_accumulate_bf16(dbuf[off:], sbuf[off:], seed=p["seed"], step=step)
+        torch.cuda.synchronize()
+        ORC.sr_accumulate_bf16(dst, src, seed=p["seed"], step=step)
+        assert_bits_equal(to_host(dbuf[off:]), dst, f"dst, micro-step {t}")
+        assert not to_host(sbuf).any(), f"source not zeroed, micro-step {t}"
+        assert not to_host(dbuf[:off]).any(), "write before the destination"
