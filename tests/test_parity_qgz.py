@@ -318,3 +318,45 @@ def test_subnormal_sums_parity(dev, R, G, B):
         binding.dequant_reduce(to_dev(c2, dev), to_dev(s2, dev), outf, N, R, G, B)
         torch.cuda.synchronize()
         assert_bits_equal(to_host(outf), ORC.dequant_reduce(c2, s2, N, R, G, B), "hop-2 sums")
+
+
+SIGNED_ZERO_SCALES = np.array([0.0, -0.0, 2.0 ** -149, -(2.0 ** -149), 3 * 2.0 ** -149, -1.5,
+                               2.0 ** -127, 1.0, -(2.0 ** -126), 1e30], np.float32)
+
+
+@pytest.mark.parametrize("R,G,B", [(1, 1, 256), (2, 1, 64), (8, 1, 256), (5, 1, 32),
+                                   (16, 2, 512), (8, 2, 256), (4, 4, 128)])
+def test_zero_and_negative_scales_parity(dev, R, G, B):
+    """Every reduce sum starts at +0 and adds fl(q * scale) in source order.
+    Scales of +-0 with nonzero codes make products of -0, which +0 turns into
+    +0, and negative and subnormal scales down to 2^-149 make tiny nonzero
+    products.  The quantizer never writes such scales, but the reduce's
+    definition covers them, and the kernels' first-term shortcut must match
+    it for every one of them.  (|q * scale| stays below 8e30: no infinities.)"""
+    N = R * B * 4
+    rng = np.random.default_rng(R * 97 + B)
+    codes = rng.integers(0, 256, size=R * N // 2, dtype=np.uint8)
+    scales = rng.choice(SIGNED_ZERO_SCALES, size=R * N // B).astype(np.float32)
+    # the first block of every source buffer (what shard 0 reads first, flat
+    # or second hop) gets a zero scale of alternating sign: all-zero sums
+    scales[np.arange(R) * (N // B)] = np.where(np.arange(R) % 2 == 0, np.float32(0.0),
+                                               np.float32(-0.0))
+    cd, sd = to_dev(codes, dev), to_dev(scales, dev)
+    # the reduce reads R source buffers (flat) or G (second hop) of N codes each
+    nsrc = R if G == 1 else G
+    c2, s2 = codes[:nsrc * N // 2], scales[:nsrc * N // B]
+    for out_bf16 in (False, True):
+        out = torch.empty(N, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
+        binding.dequant_reduce(to_dev(c2, dev), to_dev(s2, dev), out, N, R, G, B)
+        torch.cuda.synchronize()
+        want = ORC.dequant_reduce(c2, s2, N, R, G, B, 1.0, out_bf16)
+        assert_bits_equal(to_host(out), want, f"sums, {'bf16' if out_bf16 else 'fp32'}")
+        if not out_bf16:
+            assert np.all(want[:B].view(np.uint32) == 0), "shard 0's first block must be +0"
+    c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    binding.dequant_reduce_requant(cd, sd, c1, s1, N, R, G, B)
+    torch.cuda.synchronize()
+    oc1, os1 = ORC.dequant_reduce_requant(codes, scales, N, R, G, B)
+    assert_bits_equal(to_host(c1), oc1, "first-hop codes")
+    assert_bits_equal(to_host(s1), os1, "first-hop scales")

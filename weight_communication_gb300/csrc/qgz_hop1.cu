@@ -17,7 +17,8 @@
 // reads L codes and scales (L/2 + 4L/B bytes) and writes half a byte: at L = 8
 // it does about 40 fp32/int operations per 4.6 bytes, so it is issue-bound,
 // and the work goes into keeping the instruction count per code at its floor
-// (one byte permute and three exact fp32 operations).
+// (one byte permute and three exact fp32 operations, two for the first
+// source, whose add to the +0 start folds into one fma).
 //
 // Fast path (B = 256, 512, 1024 and L a power of two up to 16): one warp per
 // output block, lane t owning outputs t*B/32 .. t*B/32 + B/32 - 1, the source
@@ -176,15 +177,15 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
     }
     float p[E];
 #pragma unroll
-    for (int j = 0; j < E; ++j) p[j] = 0.0f;
-#pragma unroll
     for (int t = 0; t < L; ++t) {
 #pragma unroll
         for (int wq = 0; wq < W; ++wq) {
             float f[8];
             unpack_int4x8(w[t][wq], f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) p[8 * wq + j] = __fadd_rn(p[8 * wq + j], dequant(f[j], sc[t]));
+            for (int j = 0; j < 8; ++j)
+                p[8 * wq + j] = t == 0 ? dequant_first(f[j], sc[t])
+                                       : __fadd_rn(p[8 * wq + j], dequant(f[j], sc[t]));
         }
     }
     const bool out_ok = WC_IN_BOUNDS(uint64_t(o) + E <= uint64_t(geo.G) * geo.N);

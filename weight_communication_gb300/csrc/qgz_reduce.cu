@@ -16,7 +16,8 @@
 // The per-code work -- unpack, multiply by the scale, add in source order --
 // is all the kernel does besides moving bytes, so it runs issue-bound unless
 // the instruction count per code stays near its floor of one byte permute
-// and three exact fp32 operations.  Hence: the source count is a template
+// and three exact fp32 operations (two for the first source, whose add to
+// the +0 start folds into one fma).  Hence: the source count is a template
 // parameter (no loop bounds, no guards, every load hoisted ahead of the
 // adds), each thread makes 16 consecutive outputs from one 8-byte code word
 // per source (so the per-source address and scale work is amortized over 16
@@ -56,15 +57,19 @@ __device__ __forceinline__ void store16(void *out, uint32_t o, const float acc[1
     }
 }
 
-// acc[0..16) += the 16 codes of w (element 2k in the low nibble of byte k) * sc
+// acc[0..16) += the 16 codes of w (element 2k in the low nibble of byte k) * sc;
+// FIRST: acc is +0 (the sums' start), so the add folds into one fma.
+template <bool FIRST = false>
 __device__ __forceinline__ void accumulate16(uint2 w, float sc, float acc[16]) {
     float f[8];
     unpack_int4x8(w.x, f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], dequant(f[j], sc));
+    for (int j = 0; j < 8; ++j)
+        acc[j] = FIRST ? dequant_first(f[j], sc) : __fadd_rn(acc[j], dequant(f[j], sc));
     unpack_int4x8(w.y, f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[8 + j] = __fadd_rn(acc[8 + j], dequant(f[j], sc));
+    for (int j = 0; j < 8; ++j)
+        acc[8 + j] = FIRST ? dequant_first(f[j], sc) : __fadd_rn(acc[8 + j], dequant(f[j], sc));
 }
 
 // First code position and scale index of destination k's 16 outputs at i.
@@ -116,10 +121,9 @@ dequant_reduce_fixed_kernel(const uint8_t *__restrict__ codes, const float *__re
         }
     }
     float acc[16];
+    accumulate16<true>(w[0], sc[0], acc);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-#pragma unroll
-    for (int t = 0; t < NSRC; ++t) accumulate16(w[t], sc[t], acc);
+    for (int t = 1; t < NSRC; ++t) accumulate16(w[t], sc[t], acc);
     if (WC_IN_BOUNDS(output_in_bounds(geo, k, i)))
         store16<OUT_BF16, SCALED>(out, k * geo.S + i, acc, out_scale);
 }

@@ -151,6 +151,17 @@ __device__ __forceinline__ QCode quant_code(float x, const BlockScale &s) {
 // Dequantized value: code * scale, one rounding.
 __device__ __forceinline__ float dequant(float q, float scale) { return __fmul_rn(q, scale); }
 
+// First term of a sum that starts at +0: (+0) + fl(q * scale), two roundings,
+// equals fma(q, scale, +0), one rounding, for every integer-valued q and
+// every scale.  If q * scale is exactly zero, both sums are +0 (a sum of
+// zeros of opposite sign rounds to +0).  Otherwise |q * scale| >= |scale| is
+// at least the smallest subnormal, so it rounds to a nonzero r.  Adding +0
+// to r is exact, and the fma rounds q * scale + 0 = q * scale once, to r.
+// One instruction instead of two.
+__device__ __forceinline__ float dequant_first(float q, float scale) {
+    return __fmaf_rn(q, scale, 0.0f);
+}
+
 // Unpacking: a biased code u in [0, 2^k) placed in the mantissa of 2^23 reads
 // as 2^23 + u exactly; subtracting 2^23 + bias leaves the signed code, exact.
 // PRMT (byte permute) moves byte `b` of x under the exponent byte 0x4B.
