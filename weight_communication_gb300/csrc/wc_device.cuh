@@ -88,13 +88,21 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2_bits(float lo, float hi) {
     return bits;
 }
 
-// Max over the `width` lanes of an aligned lane group (width a power of two).
+// Max over the `width` lanes of an aligned lane group (width a power of two)
+// of values v >= +0 that are not NaN -- every caller reduces absolute values.
+// For such floats the order of the encodings, read as unsigned integers, is
+// the order of the values, so a whole warp reduces with one integer max
+// (redux.sync); narrower groups use shuffles.
 template <int WIDTH>
 __device__ __forceinline__ float group_max(float v) {
+    if constexpr (WIDTH == kWarp) {
+        return __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(v)));
+    } else {
 #pragma unroll
-    for (int off = WIDTH / 2; off > 0; off >>= 1)
-        v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
-    return v;
+        for (int off = WIDTH / 2; off > 0; off >>= 1)
+            v = fmaxf(v, __shfl_xor_sync(kFull, v, off));
+        return v;
+    }
 }
 
 // Scale and reciprocal of a symmetric block: a block whose scale m / qmax
