@@ -117,6 +117,19 @@ def test_binding_rejects_cpu_tensors(lib):
                               torch.zeros(4), 256, 4, 1, 256)
 
 
+def test_binding_rejects_a_stream_of_another_gpu():
+    """A stream must belong to the tensors' GPU: a launch on another GPU's
+    stream would fail in the driver, so the binding refuses it first."""
+    import types
+    import torch
+    t = torch.empty(0, device="meta")
+    other = types.SimpleNamespace(device=torch.device("cuda", 1), cuda_stream=0)
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        binding._stream(t, other)
+    same = types.SimpleNamespace(device=t.device, cuda_stream=1234)
+    assert binding._stream(t, same).value == 1234
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         binding.load(tmp_path / "libwc.so")

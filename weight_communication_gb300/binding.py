@@ -113,8 +113,13 @@ def _call(device: torch.device, name: str, *args) -> None:
 
 
 def _stream(t: torch.Tensor, stream: torch.cuda.Stream | None):
-    s = stream if stream is not None else torch.cuda.current_stream(t.device)
-    return ctypes.c_void_p(s.cuda_stream)
+    """The launch stream: `stream`, which must belong to the tensors' GPU, or
+    that GPU's current stream."""
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+    if stream.device != t.device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {t.device}")
+    return ctypes.c_void_p(stream.cuda_stream)
 
 
 def _dev(t: torch.Tensor | None, name: str, dtype: torch.dtype, numel: int, device=None):
