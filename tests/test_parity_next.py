@@ -212,16 +212,30 @@ def test_reducer_with_first_hop_error_feedback_matches_oracle(dev):
         assert_bits_equal(to_host(red.ef1), e1, f"first-hop error step {t}")
 
 
-def test_device_pipeline_matches_serial_steps(dev):
+EF_BITS = {torch.float32: torch.int32, torch.bfloat16: torch.int16, torch.int8: torch.int8}
+
+
+def _same_state(a, b, what):
+    """The reducers' error buffers (with the int8 buffer's scales and the
+    first-hop errors) are equal bit for bit."""
+    assert torch.equal(a.ef.view(EF_BITS[a.ef.dtype]), b.ef.view(EF_BITS[b.ef.dtype])), what
+    if a.ef_scales is not None:
+        assert torch.equal(a.ef_scales.view(torch.int32), b.ef_scales.view(torch.int32)), what
+    if a.ef1 is not None:
+        assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32)), what
+
+
+@pytest.mark.parametrize("ef_dtype", [torch.float32, torch.bfloat16, torch.int8])
+def test_device_pipeline_matches_serial_steps(dev, ef_dtype):
     """Steps with the reduce on a second stream give the same shards, error
     buffers and (hierarchical) first-hop errors as serial steps."""
     from weight_communication_gb300.qgz import DevicePipeline, QgzReducer
     for w in (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 64), wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 8)):
         out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
         a = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
-                       hop1_ef=w.G > 1)
+                       ef_dtype=ef_dtype, hop1_ef=w.G > 1)
         b = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
-                       hop1_ef=w.G > 1)
+                       ef_dtype=ef_dtype, hop1_ef=w.G > 1)
         pipe = DevicePipeline(a)
         grads = [wl.qgz_gradients(w, t, device=dev) for t in range(5)]
         outs = []
@@ -236,21 +250,20 @@ def test_device_pipeline_matches_serial_steps(dev):
             want = b.step(grads[t])
             assert torch.equal(outs[t].view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32),
                                want.view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32)), t
-        assert torch.equal(a.ef.view(torch.int32), b.ef.view(torch.int32))
-        if w.G > 1:
-            assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32))
+        _same_state(a, b, w.name)
 
 
-def test_graphed_step_matches_eager_steps(dev):
+@pytest.mark.parametrize("ef_dtype", [torch.float32, torch.bfloat16, torch.int8])
+def test_graphed_step_matches_eager_steps(dev, ef_dtype):
     """A step captured in a CUDA graph and replayed gives, step after step,
     the same shards, error buffers and first-hop errors as eager steps."""
     from weight_communication_gb300.qgz import GraphedStep, QgzReducer
     for w in (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 16), wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 4)):
         out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
         a = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
-                       hop1_ef=w.G > 1)
+                       ef_dtype=ef_dtype, hop1_ef=w.G > 1)
         b = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype, device=dev,
-                       hop1_ef=w.G > 1)
+                       ef_dtype=ef_dtype, hop1_ef=w.G > 1)
         graphed = GraphedStep(a)
         assert not a.ef.any(), "capturing must not run the step"
         view = torch.int16 if out_dtype == torch.bfloat16 else torch.int32
@@ -261,6 +274,4 @@ def test_graphed_step_matches_eager_steps(dev):
             want = b.step(g)
             torch.cuda.synchronize()
             assert torch.equal(got.view(view), want.view(view)), (w.name, t)
-            assert torch.equal(a.ef.view(torch.int32), b.ef.view(torch.int32)), (w.name, t)
-            if w.G > 1:
-                assert torch.equal(a.ef1.view(torch.int32), b.ef1.view(torch.int32)), (w.name, t)
+            _same_state(a, b, (w.name, t))
