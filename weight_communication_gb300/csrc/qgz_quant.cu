@@ -12,8 +12,8 @@
 // with kernel fusion.
 //
 // One warp owns one quantization block (or, for blocks shorter than the warp
-// tile, each aligned group of lanes owns one block), so the absmax is a
-// warp-shuffle reduction and codes, scales and the error update are produced
+// tile, each aligned group of lanes owns one block), so the absmax is a warp
+// reduction and codes, scales and the error update are produced
 // in the same pass that loads the block -- no second read, no shared memory,
 // no block barrier.  Codes are rounded and unpacked with exact fp32
 // arithmetic (wc_device.cuh), never on the conversion pipe.
@@ -35,7 +35,7 @@ namespace wc {
 // bf16 (2 bytes; the new error is rounded to the nearest bf16 when stored) or
 // int8 (1 byte, plus one fp32 scale per block: the new error of a block is
 // quantized by the int8 absmax rule once the whole block is known, so it is
-// kept in registers until a second shuffle reduction has found its maximum).
+// kept in registers until a second warp reduction has found its maximum).
 enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2, kEfInt8 = 3 };
 
 template <int B, int EF>
