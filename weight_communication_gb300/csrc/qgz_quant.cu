@@ -39,11 +39,12 @@ namespace wc {
 enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2, kEfInt8 = 3 };
 
 template <int B, int EF>
-__global__ void __launch_bounds__(256)
-ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
-                     float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
-                     float *__restrict__ scales, QgzGeometry geo, float s, float beta,
-                     float one_minus_beta) {
+__device__ __forceinline__ void ef_quant_int4_warp(const uint16_t *__restrict__ g,
+                                                   void *__restrict__ ef_v,
+                                                   float *__restrict__ ef_scales,
+                                                   uint8_t *__restrict__ codes,
+                                                   float *__restrict__ scales, QgzGeometry geo,
+                                                   float s, float beta, float one_minus_beta) {
     constexpr bool HAS_EF = EF != kEfNone;
     float *__restrict__ ef = static_cast<float *>(ef_v);
     uint16_t *__restrict__ ef16 = static_cast<uint16_t *>(ef_v);
@@ -198,6 +199,29 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
     }
 }
 
+template <int B, int EF>
+__global__ void __launch_bounds__(256)
+ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
+                     float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
+                     float *__restrict__ scales, QgzGeometry geo, float s, float beta,
+                     float one_minus_beta) {
+    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
+}
+
+// The bf16 and int8 error buffers move 2 and 1 bytes per element each way
+// instead of 4, so a warp has fewer bytes in flight; at B = 128 and 256 the
+// same code under a register budget for 8 CTAs (64 warps) per SM keeps more
+// of them resident.  (The fp32 buffer already saturates DRAM at 6 CTAs per
+// SM, and larger blocks would spill.)
+template <int B, int EF>
+__global__ void __launch_bounds__(256, 8)
+ef_quant_int4_resident8_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
+                               float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
+                               float *__restrict__ scales, QgzGeometry geo, float s, float beta,
+                               float one_minus_beta) {
+    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
+}
+
 template <int B>
 static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, float *ef_scales,
                                      uint8_t *codes, float *scales, const QgzGeometry &geo,
@@ -215,13 +239,16 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, f
         grid = dim3((tiles + threads / kWarp - 1) / (threads / kWarp));
     }
     const float omb = 1.0f - beta;
-#define WC_EFQ(MODE)                                                                       \
-    ef_quant_int4_kernel<B, MODE><<<grid, threads, 0, stream>>>(g, ef, ef_scales, codes,    \
-                                                               scales, geo, s, beta, omb)
-    if (ef == nullptr) WC_EFQ(kEfNone);
-    else if (ef_mode == kEfBf16) WC_EFQ(kEfBf16);
-    else if (ef_mode == kEfInt8) WC_EFQ(kEfInt8);
-    else WC_EFQ(kEfF32);
+    constexpr bool kResident8 = B == 128 || B == 256;
+#define WC_EFQ(KERNEL, MODE)                                                                   \
+    KERNEL<B, MODE><<<grid, threads, 0, stream>>>(g, ef, ef_scales, codes, scales, geo, s, beta, \
+                                                   omb)
+    if (ef == nullptr) WC_EFQ(ef_quant_int4_kernel, kEfNone);
+    else if (ef_mode == kEfBf16 && kResident8) WC_EFQ(ef_quant_int4_resident8_kernel, kEfBf16);
+    else if (ef_mode == kEfBf16) WC_EFQ(ef_quant_int4_kernel, kEfBf16);
+    else if (ef_mode == kEfInt8 && kResident8) WC_EFQ(ef_quant_int4_resident8_kernel, kEfInt8);
+    else if (ef_mode == kEfInt8) WC_EFQ(ef_quant_int4_kernel, kEfInt8);
+    else WC_EFQ(ef_quant_int4_kernel, kEfF32);
 #undef WC_EFQ
     return cudaPeekAtLastError();
 }
