@@ -139,8 +139,14 @@ __device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, bool out
     if (out_ok && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
 }
 
+// Launch bounds: a budget for 5 CTAs per SM (at most 51 registers) at B <= 512
+// measured faster than the compiler's unbounded choice -- at B = 512, L = 8,
+// 0.594 -> 0.574 ms without error feedback (48 registers instead of 40) and
+// 0.815 -> 0.773 ms with it (48 with 4 bytes of spills, instead of 55 and 4
+// CTAs).  A budget for 6 CTAs was slower with error feedback.  B = 1024 needs
+// about 110 registers and takes no budget.
 template <int B, int L, bool HAS_EF>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, B <= 512 ? 5 : 1)
 hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                   uint8_t *__restrict__ out_codes, float *__restrict__ out_scales,
                   QgzGeometry geo, float *__restrict__ ef1, float s, float beta,
