@@ -82,6 +82,8 @@ MUTANTS = {
     "int8ef_scale_in_send_order": ("float es8 = e8s[in0 / B];", "float es8 = e8s[out0 / B];"),
     "int8ef_beta_swapped": ("float k8 = beta * ev8[i];", "float k8 = one_mb * ev8[i];"),
     "int8ef_compensation_sign": ("c8[i] = g8 + se8;", "c8[i] = g8 - se8;"),
+    "reduce_starts_at_negative_zero": ("float acc = 0.0f;\n        if (G == 1) {",
+                                       "float acc = -0.0f;\n        if (G == 1) {"),
     "sr_step_ignored": ("uint32_t key = orc_mix32(orc_mix32(seed) ^ step);",
                         "uint32_t key = orc_mix32(orc_mix32(seed));"),
 }

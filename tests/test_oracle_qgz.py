@@ -370,3 +370,22 @@ def test_first_hop_adds_local_ranks_in_order(orc):
     assert os_[0] == ONE / np.float32(7)
     assert os_[0] != np.float32(1 + 2.0**-23) / np.float32(7)
     assert np.all(oc[:B // 2] == 0x77)
+
+
+@pytest.mark.parametrize("G", [1, 2])
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_reduce_sums_start_at_positive_zero(orc, G, out_bf16):
+    """Every reduce sum starts at +0 (IEEE: +0 + -0 = +0 when rounding to
+    nearest).  Codes of -7 with scales of +0, and codes of +1 with scales of
+    -0, give products of -0 from every source. Their sums, flat or over the
+    second hop's groups, must be +0, whose encoding is all zero bits, not -0."""
+    R, B = 4, 32
+    N = R * B * 2
+    nsrc = R if G == 1 else G
+    codes = np.full(nsrc * N // 2, 0x99, np.uint8)   # nibble 9: the code -7
+    scales = np.zeros(nsrc * N // B, np.float32)      # +0
+    codes[: N // 4] = 0x11                            # the code +1 ...
+    scales[: N // (4 * B)] = np.float32(-0.0)         # ... with scale -0
+    assert np.signbit(np.float32(-7) * scales[-1]) and np.signbit(np.float32(1) * scales[0])
+    out = orc.dequant_reduce(codes, scales, N, R, G, B, 1.0, out_bf16)
+    assert not out.view(np.uint16 if out_bf16 else np.uint32).any(), "a sum came out as -0"
