@@ -82,6 +82,17 @@ MUTANTS = {
     "int8ef_scale_in_send_order": ("float es8 = e8s[in0 / B];", "float es8 = e8s[out0 / B];"),
     "int8ef_beta_swapped": ("float k8 = beta * ev8[i];", "float k8 = one_mb * ev8[i];"),
     "int8ef_compensation_sign": ("c8[i] = g8 + se8;", "c8[i] = g8 - se8;"),
+    "ef_update_as_difference": ("float added = one_minus_beta * resid;",
+                                "float added = resid - beta * resid;"),
+    "compensation_fused": ("c[i] = gi + se;", "c[i] = fmaf(s, e[in0 + i], gi);"),
+    "scale_by_reciprocal": ("float scale = m / fq;", "float scale = m * (1.0f / fq);"),
+    "bf16ef_update_as_difference": ("float ah = omb * rh;", "float ah = rh - beta * rh;"),
+    "bf16ef_compensation_fused": ("c[i] = gh + seh;", "c[i] = fmaf(s, eh, gh);"),
+    "int8ef_update_as_difference": ("float a8 = one_mb * r8;", "float a8 = r8 - beta * r8;"),
+    "int8ef_compensation_fused": ("c8[i] = g8 + se8;", "c8[i] = fmaf(s, ev8[i], g8);"),
+    "hop1_ef_update_as_difference": ("float added1 = one_minus_beta * resid1;",
+                                     "float added1 = resid1 - beta * resid1;"),
+    "hop1_ef_compensation_fused": ("acc = acc + se1;", "acc = fmaf(s, e1[out0 + i], acc);"),
     "reduce_starts_at_negative_zero": ("float acc = 0.0f;\n        if (G == 1) {",
                                        "float acc = -0.0f;\n        if (G == 1) {"),
     "sr_step_ignored": ("uint32_t key = orc_mix32(orc_mix32(seed) ^ step);",

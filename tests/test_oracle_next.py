@@ -119,6 +119,46 @@ def test_first_hop_telescoping(orc):
     assert np.abs(e1).max() > 0
 
 
+@pytest.mark.parametrize("s,beta", [(1.0, 0.5), (0.7, 0.3)])
+def test_first_hop_error_feedback_is_the_ranks_error_feedback_chain(orc, s, beta):
+    """On partial sums that are exactly bf16 values, a unit's first hop with
+    error feedback computes what the ranks' EF-quant computes on a gradient
+    equal to those sums: the same compensation, block quantization and error
+    update, rounded in the same order (pinned by hand-worked cases of its own).
+    Codes in [-7, 7] at power-of-two scales 2^-12 .. 2^-8 make every sum of
+    the two local ranks exact and bf16-representable.  The errors are full
+    24-bit fp32 values, and s = 0.7, beta = 0.3 are not dyadic, so any other
+    rounding order shows in many elements."""
+    R, G, B, k = 4, 2, 64, 8
+    L = R // G
+    N = R * B * k
+    S = N // R
+    rng = np.random.default_rng(int(s * 10) + 7)
+    q = rng.integers(-7, 8, size=R * N)
+    codes = np.zeros(R * N // 2, np.uint8)
+    codes[:] = (q[0::2] & 15) | ((q[1::2] & 15) << 4)
+    scales = (2.0 ** -rng.integers(8, 13, size=R * N // B)).astype(np.float32)
+    d = q.astype(np.float64) * np.repeat(scales.astype(np.float64), B)
+    for g in range(G):
+        for l in range(L):
+            # partial sums of unit (g, l): sub-slice gq adds chunk l*G + gq of
+            # the group's ranks, in local-rank order
+            p = np.concatenate([sum(d[(g * L + lq) * N + (l * G + gq) * S:
+                                      (g * L + lq) * N + (l * G + gq + 1) * S] for lq in range(L))
+                                for gq in range(G)])
+            p_bf16 = _bf16(p.tolist())
+            assert np.array_equal(torch.from_numpy(p_bf16.view(np.int16)).view(torch.bfloat16)
+                                  .float().numpy().astype(np.float64), p)
+            e_start = (rng.standard_normal(G * S) * 1e-3).astype(np.float32)
+            e_hop = e_start.copy()
+            c1, s1 = orc.dequant_reduce_requant_unit_ef(codes, scales, N, R, G, B, g, l, e_hop,
+                                                        s, beta)
+            e_ref = e_start.copy()
+            c0, s0 = orc.ef_quant_int4(p_bf16, e_ref, G * S, 1, 1, B, s, beta)
+            assert np.array_equal(c1, c0) and np.array_equal(s1, s0), (g, l)
+            assert np.array_equal(e_hop.view(np.uint32), e_ref.view(np.uint32)), (g, l)
+
+
 @pytest.mark.parametrize("beta", [0.25, 0.5])
 def test_first_hop_loco_bound(orc, beta):
     w = wl.QgzWorkload(9, "t", 8, 8 * 256 * 2, 2, 256, 1.0, beta, 1, 1e-3, 1e-3, 100.0, True)
@@ -142,15 +182,22 @@ def test_first_hop_loco_bound(orc, beta):
 # bf16 error buffer
 # --------------------------------------------------------------------------
 
-def test_bf16_error_buffer_one_step_equals_rounded_fp32(orc):
-    w = wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 4)
+@pytest.mark.parametrize("n_blocks,params", [
+    (4, ((1.0, 0.5), (1.0, 0.0), (0.5, 0.25))),
+    # s and beta that are not dyadic: another rounding order of the chain
+    # changes the fp32 error by an ulp in many elements, and over 2 M elements
+    # some of those changes cross a bf16 rounding boundary
+    (128, ((0.7, 0.3),)),
+])
+def test_bf16_error_buffer_one_step_equals_rounded_fp32(orc, n_blocks, params):
+    w = wl.QGZ_SINGLE_HOP.scaled(8 * 256 * n_blocks)
     g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
     rng = np.random.default_rng(4)
     e_start = torch.from_numpy((rng.standard_normal(w.R * w.N) * 1e-4).astype(np.float32)) \
         .to(torch.bfloat16)
     e16 = wl.as_u16(e_start).copy()
     e32 = e_start.float().numpy().copy()
-    for s, beta in ((1.0, 0.5), (1.0, 0.0), (0.5, 0.25)):
+    for s, beta in params:
         a16, a32 = e16.copy(), e32.copy()
         c16, s16 = orc.ef_quant_int4_bf16ef(g, a16, w.N, w.R, w.G, w.B, s, beta)
         c32, s32 = orc.ef_quant_int4(g, a32, w.N, w.R, w.G, w.B, s, beta)
@@ -221,19 +268,25 @@ def test_int8_error_buffer_worked_example(orc):
     assert 0.25 < e8s[0] * 127 < 0.252
 
 
-@pytest.mark.parametrize("G", [1, 2])
-def test_int8_error_buffer_one_step_equals_quantized_fp32(orc, G):
+@pytest.mark.parametrize("G,n_blocks,params", [
+    (1, 3, ((1.0, 0.5), (0.5, 0.25))),
+    (2, 3, ((1.0, 0.5), (0.5, 0.25))),
+    # not dyadic: over 2 M elements some ulp changes of the fp32 error from
+    # another rounding order cross an int8 rounding boundary
+    (1, 128, ((0.7, 0.3),)),
+])
+def test_int8_error_buffer_one_step_equals_quantized_fp32(orc, G, n_blocks, params):
     """From the same stored error, one step gives the fp32-buffer step's codes
     and scales, and stores exactly the int8 block quantization (the pinned
     qwZ rule) of the fp32 step's new error, block by block in gradient order."""
     R, B = 8, 256
-    w = wl.QgzWorkload(9, "t", R, R * B * 3, G, B, 1.0, 0.5, 1, 1e-3, 1e-3, 100.0, False)
+    w = wl.QgzWorkload(9, "t", R, R * B * n_blocks, G, B, 1.0, 0.5, 1, 1e-3, 1e-3, 100.0, False)
     g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
     rng = np.random.default_rng(G)
     e8 = rng.integers(-127, 128, size=R * w.N).astype(np.int8)
     e8s = (rng.random(R * w.N // B) * 1e-6).astype(np.float32)
     e32 = (e8.astype(np.float32) * np.repeat(e8s, B)).astype(np.float32)   # code * scale, one rounding
-    for s, beta in ((1.0, 0.5), (0.5, 0.25)):
+    for s, beta in params:
         a8, a8s, a32 = e8.copy(), e8s.copy(), e32.copy()
         c8, s8 = orc.ef_quant_int4_int8ef(g, a8, a8s, w.N, R, G, B, s, beta)
         c32, s32 = orc.ef_quant_int4(g, a32, w.N, R, G, B, s, beta)

@@ -113,6 +113,40 @@ def test_plain_error_feedback_keeps_residual(orc):
     assert unpack_int4(codes).tolist() == [0, 7, 0, 0]
 
 
+def test_error_update_rounds_as_stated(orc):
+    """e' = fl(fl(beta*e) + fl(fl(1 - beta) * fl(c - d))): (1 - beta) is formed
+    once and multiplies the residual.  Worked by hand, beta = 0.75, s = 1, B = 2:
+      g = (2, 28), e = (-1 + 2^-23, 0)  ->  c = (1 + 2^-23, 28), exact;
+      m = 28, scale = 4, inv = 0.25; c*inv = (0.25 + 2^-25, 7), q = (0, 7);
+      residual r = 1 + 2^-23 and (1 - beta)*r = 0.25 + 2^-25, exact;
+      beta*e = -0.75 + 1.5*2^-24 lies halfway between floats 2^-24 apart, and
+      ties to even give -0.75 + 2^-23;
+      e'_0 = -0.75 + 2^-23 + 0.25 + 2^-25 = -0.5 + 5*2^-25, exact.
+    The algebraically equal r - beta*r rounds beta*r = 0.75 + 1.5*2^-24 to
+    0.75 + 2^-23, leaves 0.25, and would give e'_0 = -0.5 + 2^-23."""
+    g = _bf16_bits([2.0, 28.0])
+    e = np.array([-1.0 + 2.0 ** -23, 0.0], dtype=np.float32)
+    codes, scales = orc.ef_quant_int4(g, e, 2, 1, 1, 2, 1.0, 0.75)
+    assert unpack_int4(codes).tolist() == [0, 7]
+    assert scales.tolist() == [4.0]
+    assert e[0] == np.float32(-0.5 + 5 * 2.0 ** -25)
+    assert e[1] == 0.0
+
+
+def test_compensation_rounds_the_product_first(orc):
+    """c = fl(g + fl(s*e)).  With s = 3, e = 1 + 2^-23 and g = -3:
+    s*e = 3 + 1.5*2^-22 lies halfway between floats 2^-22 apart, ties to even
+    give 3 + 2^-21, and c = 2^-21 exactly (a fused multiply-add would give
+    1.5*2^-22).  The block's maximum is then 2^-21, its scale fl(2^-21 / 7),
+    and c quantizes to the code 7."""
+    g = _bf16_bits([-3.0, 0.0])
+    e = np.array([1.0 + 2.0 ** -23, 0.0], dtype=np.float32)
+    codes, scales = orc.ef_quant_int4(g, e, 2, 1, 1, 2, 3.0, 0.0)
+    assert unpack_int4(codes).tolist() == [7, 0]
+    assert scales[0] == np.float32(2.0 ** -21) / np.float32(7)
+    assert scales[0] != np.float32(1.5 * 2.0 ** -22) / np.float32(7)
+
+
 def test_error_scale_zero_and_null_buffer_quantize_g_alone(orc):
     w = wl.QGZ_TINY.scaled(8192)
     g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
