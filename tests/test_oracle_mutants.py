@@ -93,8 +93,13 @@ MUTANTS = {
     "hop1_ef_update_as_difference": ("float added1 = one_minus_beta * resid1;",
                                      "float added1 = resid1 - beta * resid1;"),
     "hop1_ef_compensation_fused": ("acc = acc + se1;", "acc = fmaf(s, e1[out0 + i], acc);"),
+    "code_from_exact_product": ("float r = rintf(t);", "float r = (float)rint((double)x[i] * inv);"),
+    "bf16_output_unscaled": ("float v = acc * out_scale;",
+                             "float v = out_bf16 ? acc : acc * out_scale;"),
     "reduce_starts_at_negative_zero": ("float acc = 0.0f;\n        if (G == 1) {",
                                        "float acc = -0.0f;\n        if (G == 1) {"),
+    "sr_compare_form": ("return (uint16_t)((u + r) >> 16);",
+                        "return (uint16_t)((u >> 16) + ((u & 0xFFFFu) > r ? 1u : 0u));"),
     "sr_step_ignored": ("uint32_t key = orc_mix32(orc_mix32(seed) ^ step);",
                         "uint32_t key = orc_mix32(orc_mix32(seed));"),
 }

@@ -147,6 +147,22 @@ def test_compensation_rounds_the_product_first(orc):
     assert scales[0] != np.float32(1.5 * 2.0 ** -22) / np.float32(7)
 
 
+def test_code_rounds_the_product_before_rint(orc):
+    """q = rint(fl(c*inv)): the product is rounded to fp32 first.  Block
+    (c0, m) = (1.5 + 5*2^-23, 7 + 3*2^-20), made exact as c = 0 + 1*e:
+      inv = fl(7/m) = 1 - 7*2^-24 (7/m = 1 - 6.86*2^-24 + ...);
+      c0*inv = 1.5 - 2^-25 - 35*2^-47 exactly, within half an ulp (2^-24) of
+      1.5, so fl(c0*inv) = 1.5 and rint ties it to the even 2; rounding the
+      exact product straight to an integer would give 1;
+      m*inv = 7 - 2^-24 - ..., fl = 7, q = 7; scale = fl(m/7) = 1 + 3*2^-23."""
+    c = np.array([1.5 + 5 * 2.0 ** -23, 7 + 3 * 2.0 ** -20], np.float32)
+    g = _bf16_bits([0.0, 0.0])
+    e = c.copy()
+    codes, scales = orc.ef_quant_int4(g, e, 2, 1, 1, 2, 1.0, 0.0)
+    assert unpack_int4(codes).tolist() == [2, 7]
+    assert scales[0] == np.float32(1 + 3 * 2.0 ** -23)
+
+
 def test_error_scale_zero_and_null_buffer_quantize_g_alone(orc):
     w = wl.QGZ_TINY.scaled(8192)
     g = wl.as_u16(wl.qgz_gradients(w, 0)).ravel().copy()
@@ -423,3 +439,16 @@ def test_reduce_sums_start_at_positive_zero(orc, G, out_bf16):
     assert np.signbit(np.float32(-7) * scales[-1]) and np.signbit(np.float32(1) * scales[0])
     out = orc.dequant_reduce(codes, scales, N, R, G, B, 1.0, out_bf16)
     assert not out.view(np.uint16 if out_bf16 else np.uint32).any(), "a sum came out as -0"
+
+
+def test_output_scale_applies_before_bf16_rounding(orc):
+    """out = bf16_rn(fl(sum * out_scale)), flat and second hop: codes 7 at
+    scale 1 sum to 7 per source; with out_scale 0.5 one source gives 3.5
+    (bf16 0x4060) and two give 7 (0x40E0), never the unscaled 7 and 14."""
+    one = orc.dequant_reduce(np.full(1, 0x77, np.uint8), np.ones(1, np.float32), 2, 1, 1, 2,
+                             0.5, True)
+    assert one.tolist() == [0x4060, 0x4060]
+    two = orc.dequant_reduce(np.full(4, 0x77, np.uint8), np.ones(4, np.float32), 4, 2, 2, 2,
+                             0.5, True)
+    assert two.tolist() == [0x40E0] * 4
+

@@ -86,6 +86,21 @@ def test_sr_is_exactly_unbiased_over_all_r(orc, bits):
     assert len(counts) <= 2                      # only the two neighbours
 
 
+def test_sr_rounds_by_the_carry(orc):
+    """The carry form: bf16 = (bits(x) + r) >> 16, so x rounds its magnitude up
+    exactly when its low 16 bits plus r reach 2^16.  x = 1 + 2^-8 has the
+    encoding 0x3F808000, low half 0x8000: r = 0x8000 carries (0x3F81, up) and
+    r = 0x7FFF does not (0x3F80, down).  The other unbiased form, "up when the
+    low half exceeds r", gives the opposite at both.  Negative values round
+    their magnitude the same way; infinity passes through."""
+    x = float(np.float32(1 + 2.0 ** -8))
+    assert orc.sr_round(x, 0x8000) == 0x3F81
+    assert orc.sr_round(x, 0x7FFF) == 0x3F80
+    assert orc.sr_round(-x, 0x8000) == 0xBF81
+    assert orc.sr_round(-x, 0x7FFF) == 0xBF80
+    assert orc.sr_round(float("inf"), 0xFFFF) == 0x7F80
+
+
 def test_sr_empirical_mean_over_seeds(orc):
     x = _f32(0x3F80_5A3C)                        # p = 0x5A3C / 65536
     lo, hi = frac_of_bf16_bits(0x3F80), frac_of_bf16_bits(0x3F81)
