@@ -85,14 +85,6 @@ def max_over_ranks(value: float, dist, device) -> float:
     return float(t.item())
 
 
-def sum_over_ranks(value: float, dist, device) -> float:
-    if dist is None:
-        return value
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
-
-
 def job_throughput(units_per_rank_step: float, ws: int, max_ms_per_step: float) -> float:
     """Whole-job rate: every replica processes the same units per step and
     the job advances at the pace of the slowest rank."""
