@@ -58,26 +58,28 @@ _U32 = ctypes.c_uint32
 _U16 = ctypes.c_uint16
 
 _SIGS = {
+    "orc_max_block": (_I, []),
     "orc_bf16_to_f32": (ctypes.c_float, [_U16]),
     "orc_f32_to_bf16_rne": (_U16, [_F]),
     "orc_quant_block": (None, [_P, _I, _I, _P, _P]),
     "orc_dequant": (ctypes.c_float, [_I, _F]),
     "orc_get_nibble": (_I, [_P, _I64]),
     "orc_send_position": (_I64, [_I64, _I, _I]),
-    "orc_ef_quant_int4_rank": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
-    "orc_ef_quant_int4": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_rank": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
     "orc_dequant_reduce_dest": (None, [_P, _P, _I64, _I, _I, _I, _I, _F, _P, _I]),
+    "orc_dequant_reduce_dest_range": (None, [_P, _P, _I64, _I, _I, _I, _I, _I64, _I64, _F, _P, _I]),
     "orc_dequant_reduce": (None, [_P, _P, _I64, _I, _I, _I, _F, _P, _I]),
-    "orc_dequant_reduce_requant_unit": (None, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P]),
-    "orc_dequant_reduce_requant": (None, [_P, _P, _I64, _I, _I, _I, _P, _P]),
-    "orc_dequant_reduce_requant_unit_ef": (None, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _P, _F, _F]),
-    "orc_dequant_reduce_requant_ef": (None, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F]),
-    "orc_ef_quant_int4_rank_bf16ef": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
-    "orc_ef_quant_int4_bf16ef": (None, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
-    "orc_ef_quant_int4_rank_int8ef": (None, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
-    "orc_ef_quant_int4_int8ef": (None, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
-    "orc_qwz_quant_replica_int8": (None, [_P, _P, _P, _P, _I64, _I]),
-    "orc_qwz_quant_int8": (None, [_P, _P, _P, _I64, _I]),
+    "orc_dequant_reduce_requant_unit": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P]),
+    "orc_dequant_reduce_requant": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P]),
+    "orc_dequant_reduce_requant_unit_ef": (_I, [_P, _P, _I64, _I, _I, _I, _I, _I, _P, _P, _P, _F, _F]),
+    "orc_dequant_reduce_requant_ef": (_I, [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F]),
+    "orc_ef_quant_int4_rank_bf16ef": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_bf16ef": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_rank_int8ef": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_ef_quant_int4_int8ef": (_I, [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F]),
+    "orc_qwz_quant_replica_int8": (_I, [_P, _P, _P, _P, _I64, _I]),
+    "orc_qwz_quant_int8": (_I, [_P, _P, _P, _I64, _I]),
     "orc_qwz_dequant_int8": (None, [_P, _P, _P, _I64, _I]),
     "orc_fmix32": (_U32, [_U32]),
     "orc_mix32": (_U32, [_U32]),
@@ -87,6 +89,15 @@ _SIGS = {
 }
 
 MAX_BLOCK = 8192  # the oracle's per-block scratch holds this many values
+EBLOCK = -1       # status of a C call refused for a block size outside [1, MAX_BLOCK]
+
+
+def _status(rc: int, name: str) -> None:
+    """The C functions with per-block scratch check B themselves and return a
+    nonzero status, having written nothing, when it is out of range."""
+    if rc != 0:
+        raise ValueError(f"{name} refused the call (status {rc}): block size outside "
+                         f"[1, {MAX_BLOCK}]")
 
 
 def _ptr(a: np.ndarray | None):
@@ -182,8 +193,8 @@ class Oracle:
             assert ef.dtype == np.float32 and ef.size == R * N
         codes = np.zeros(R * N // 2, dtype=np.uint8)
         scales = np.zeros(R * N // B, dtype=np.float32)
-        self._lib.orc_ef_quant_int4(_ptr(g), _ptr(ef), _ptr(codes), _ptr(scales),
-                                    N, R, G, B, s, beta)
+        _status(self._lib.orc_ef_quant_int4(_ptr(g), _ptr(ef), _ptr(codes), _ptr(scales),
+                                    N, R, G, B, s, beta), "orc_ef_quant_int4")
         return codes, scales
 
     def ef_quant_int4_rank(self, g_r: np.ndarray, ef_r: np.ndarray | None, N: int,
@@ -193,8 +204,8 @@ class Oracle:
         assert g_r.dtype == np.uint16 and g_r.size == N
         codes = np.zeros(N // 2, dtype=np.uint8)
         scales = np.zeros(N // B, dtype=np.float32)
-        self._lib.orc_ef_quant_int4_rank(_ptr(g_r), _ptr(ef_r), _ptr(codes),
-                                         _ptr(scales), N, R, G, B, s, beta)
+        _status(self._lib.orc_ef_quant_int4_rank(_ptr(g_r), _ptr(ef_r), _ptr(codes),
+                                         _ptr(scales), N, R, G, B, s, beta), "orc_ef_quant_int4_rank")
         return codes, scales
 
     def dequant_reduce(self, codes, scales, N, R, G, B, out_scale=1.0, out_bf16=False):
@@ -214,13 +225,24 @@ class Oracle:
                                           out_scale, _ptr(out), int(out_bf16))
         return out
 
+    def dequant_reduce_dest_range(self, codes, scales, N, R, G, B, k, i0, i1, out_scale=1.0,
+                                  out_bf16=False):
+        """Outputs [i0, i1) of destination k; returns [i1 - i0]."""
+        S, _, _ = _check_qgz(N, R, G, B)
+        if not 0 <= i0 <= i1 <= S:
+            raise ValueError(f"need 0 <= i0 <= i1 <= S={S} (i0={i0}, i1={i1})")
+        out = np.zeros(i1 - i0, dtype=np.uint16 if out_bf16 else np.float32)
+        self._lib.orc_dequant_reduce_dest_range(_ptr(codes), _ptr(scales), N, R, G, B, k, i0, i1,
+                                                out_scale, _ptr(out), int(out_bf16))
+        return out
+
     def dequant_reduce_requant(self, codes, scales, N, R, G, B):
         """Hop 1, every unit.  Returns (codes [R*G*S/2], scales [R*G*S/B])."""
         S, _, _ = _check_qgz(N, R, G, B)
         oc = np.zeros(R * G * S // 2, dtype=np.uint8)
         os_ = np.zeros(R * G * S // B, dtype=np.float32)
-        self._lib.orc_dequant_reduce_requant(_ptr(codes), _ptr(scales), N, R, G, B,
-                                             _ptr(oc), _ptr(os_))
+        _status(self._lib.orc_dequant_reduce_requant(_ptr(codes), _ptr(scales), N, R, G, B,
+                                             _ptr(oc), _ptr(os_)), "orc_dequant_reduce_requant")
         return oc, os_
 
     def dequant_reduce_requant_unit(self, codes, scales, N, R, G, B, g, l):
@@ -228,8 +250,8 @@ class Oracle:
         S, _, _ = _check_qgz(N, R, G, B)
         oc = np.zeros(G * S // 2, dtype=np.uint8)
         os_ = np.zeros(G * S // B, dtype=np.float32)
-        self._lib.orc_dequant_reduce_requant_unit(_ptr(codes), _ptr(scales), N, R, G,
-                                                  B, g, l, _ptr(oc), _ptr(os_))
+        _status(self._lib.orc_dequant_reduce_requant_unit(_ptr(codes), _ptr(scales), N, R, G,
+                                                  B, g, l, _ptr(oc), _ptr(os_)), "orc_dequant_reduce_requant_unit")
         return oc, os_
 
     def dequant_reduce_requant_ef(self, codes, scales, N, R, G, B, e1, s, beta):
@@ -240,8 +262,8 @@ class Oracle:
             assert e1.dtype == np.float32 and e1.size == R * G * S
         oc = np.zeros(R * G * S // 2, dtype=np.uint8)
         os_ = np.zeros(R * G * S // B, dtype=np.float32)
-        self._lib.orc_dequant_reduce_requant_ef(_ptr(codes), _ptr(scales), N, R, G, B,
-                                                _ptr(oc), _ptr(os_), _ptr(e1), s, beta)
+        _status(self._lib.orc_dequant_reduce_requant_ef(_ptr(codes), _ptr(scales), N, R, G, B,
+                                                _ptr(oc), _ptr(os_), _ptr(e1), s, beta), "orc_dequant_reduce_requant_ef")
         return oc, os_
 
     def dequant_reduce_requant_unit_ef(self, codes, scales, N, R, G, B, g, l, e1u, s, beta):
@@ -249,9 +271,9 @@ class Oracle:
         S, _, _ = _check_qgz(N, R, G, B)
         oc = np.zeros(G * S // 2, dtype=np.uint8)
         os_ = np.zeros(G * S // B, dtype=np.float32)
-        self._lib.orc_dequant_reduce_requant_unit_ef(_ptr(codes), _ptr(scales), N, R, G, B,
+        _status(self._lib.orc_dequant_reduce_requant_unit_ef(_ptr(codes), _ptr(scales), N, R, G, B,
                                                      g, l, _ptr(oc), _ptr(os_), _ptr(e1u),
-                                                     s, beta)
+                                                     s, beta), "orc_dequant_reduce_requant_unit_ef")
         return oc, os_
 
     def ef_quant_int4_bf16ef(self, g: np.ndarray, e16: np.ndarray, N: int, R: int, G: int,
@@ -262,16 +284,16 @@ class Oracle:
         assert e16.dtype == np.uint16 and e16.size == R * N
         codes = np.zeros(R * N // 2, dtype=np.uint8)
         scales = np.zeros(R * N // B, dtype=np.float32)
-        self._lib.orc_ef_quant_int4_bf16ef(_ptr(g), _ptr(e16), _ptr(codes), _ptr(scales),
-                                           N, R, G, B, s, beta)
+        _status(self._lib.orc_ef_quant_int4_bf16ef(_ptr(g), _ptr(e16), _ptr(codes), _ptr(scales),
+                                           N, R, G, B, s, beta), "orc_ef_quant_int4_bf16ef")
         return codes, scales
 
     def ef_quant_int4_rank_bf16ef(self, g_r, e16_r, N, R, G, B, s, beta):
         _check_qgz(N, R, G, B)
         codes = np.zeros(N // 2, dtype=np.uint8)
         scales = np.zeros(N // B, dtype=np.float32)
-        self._lib.orc_ef_quant_int4_rank_bf16ef(_ptr(g_r), _ptr(e16_r), _ptr(codes),
-                                                _ptr(scales), N, R, G, B, s, beta)
+        _status(self._lib.orc_ef_quant_int4_rank_bf16ef(_ptr(g_r), _ptr(e16_r), _ptr(codes),
+                                                _ptr(scales), N, R, G, B, s, beta), "orc_ef_quant_int4_rank_bf16ef")
         return codes, scales
 
     def ef_quant_int4_int8ef(self, g: np.ndarray, e8: np.ndarray, e8s: np.ndarray, N: int,
@@ -284,8 +306,8 @@ class Oracle:
         assert e8s.dtype == np.float32 and e8s.size == R * N // B
         codes = np.zeros(R * N // 2, dtype=np.uint8)
         scales = np.zeros(R * N // B, dtype=np.float32)
-        self._lib.orc_ef_quant_int4_int8ef(_ptr(g), _ptr(e8), _ptr(e8s), _ptr(codes),
-                                           _ptr(scales), N, R, G, B, s, beta)
+        _status(self._lib.orc_ef_quant_int4_int8ef(_ptr(g), _ptr(e8), _ptr(e8s), _ptr(codes),
+                                           _ptr(scales), N, R, G, B, s, beta), "orc_ef_quant_int4_int8ef")
         return codes, scales
 
     # -- qwZ --------------------------------------------------------------
@@ -296,7 +318,7 @@ class Oracle:
         assert w.dtype == np.uint16
         codes = np.zeros(n, dtype=np.int8)
         scales = np.zeros(n // B, dtype=np.float32)
-        self._lib.orc_qwz_quant_int8(_ptr(w), _ptr(codes), _ptr(scales), n, B)
+        _status(self._lib.orc_qwz_quant_int8(_ptr(w), _ptr(codes), _ptr(scales), n, B), "orc_qwz_quant_int8")
         return codes, scales
 
     def qwz_dequant_int8(self, codes: np.ndarray, scales: np.ndarray, B: int):
@@ -313,7 +335,7 @@ class Oracle:
         codes = np.zeros(n, dtype=np.int8)
         scales = np.zeros(n // B, dtype=np.float32)
         rep = np.zeros(n, dtype=np.uint16)
-        self._lib.orc_qwz_quant_replica_int8(_ptr(w), _ptr(codes), _ptr(scales), _ptr(rep), n, B)
+        _status(self._lib.orc_qwz_quant_replica_int8(_ptr(w), _ptr(codes), _ptr(scales), _ptr(rep), n, B), "orc_qwz_quant_replica_int8")
         return codes, scales, rep
 
     # -- SR accumulate ------------------------------------------------------

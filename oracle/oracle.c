@@ -43,6 +43,20 @@
 
 #define ORC_EXPORT __attribute__((visibility("default")))
 
+/*
+ * Per-block scratch.  The functions that quantize a block at a time keep the
+ * block's values on the stack in arrays of ORC_MAX_BLOCK elements, so each
+ * of them first checks B itself: a block size outside [1, ORC_MAX_BLOCK] is
+ * refused with ORC_EBLOCK before anything is written.  They return 0 on
+ * success.
+ */
+#define ORC_MAX_BLOCK 8192
+#define ORC_EBLOCK (-1)
+
+static int orc_block_ok(int B) { return B >= 1 && B <= ORC_MAX_BLOCK; }
+
+ORC_EXPORT int orc_max_block(void) { return ORC_MAX_BLOCK; }
+
 /* ------------------------------------------------------------------------ */
 /* bfloat16 <-> binary32                                                      */
 /* ------------------------------------------------------------------------ */
@@ -187,15 +201,16 @@ ORC_EXPORT int64_t orc_send_position(int64_t slice, int R, int G)
  * scales: N/B floats.  Codes and scales come out in send order (above); the
  * error buffer stays in gradient order.
  */
-ORC_EXPORT void orc_ef_quant_int4_rank(const uint16_t *g, float *e,
+ORC_EXPORT int orc_ef_quant_int4_rank(const uint16_t *g, float *e,
                                        uint8_t *codes, float *scales,
                                        int64_t N, int R, int G, int B,
                                        float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     int64_t S = N / R;
     float one_minus_beta = 1.0f - beta;
-    float c[8192];
-    int8_t q[8192];
+    float c[ORC_MAX_BLOCK];
+    int8_t q[ORC_MAX_BLOCK];
     for (int64_t slice = 0; slice < R; ++slice) {
         int64_t p = orc_send_position(slice, R, G);
         for (int64_t b0 = 0; b0 < S; b0 += B) {
@@ -226,20 +241,23 @@ ORC_EXPORT void orc_ef_quant_int4_rank(const uint16_t *g, float *e,
             }
         }
     }
+    return 0;
 }
 
 /* All R ranks: g and e are [R][N], codes [R][N/2], scales [R][N/B]. */
-ORC_EXPORT void orc_ef_quant_int4(const uint16_t *g, float *e,
+ORC_EXPORT int orc_ef_quant_int4(const uint16_t *g, float *e,
                                   uint8_t *codes, float *scales,
                                   int64_t N, int R, int G, int B,
                                   float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     for (int r = 0; r < R; ++r)
         orc_ef_quant_int4_rank(g + (int64_t)r * N,
                                e ? e + (int64_t)r * N : 0,
                                codes + (int64_t)r * (N / 2),
                                scales + (int64_t)r * (N / B),
                                N, R, G, B, s, beta);
+    return 0;
 }
 
 /*
@@ -250,15 +268,16 @@ ORC_EXPORT void orc_ef_quant_int4(const uint16_t *g, float *e,
  * and only the new error is rounded to the nearest bf16 (ties to even) when
  * it is stored.  e16: N bf16 bit patterns, in place (not NULL).
  */
-ORC_EXPORT void orc_ef_quant_int4_rank_bf16ef(const uint16_t *g, uint16_t *e16,
+ORC_EXPORT int orc_ef_quant_int4_rank_bf16ef(const uint16_t *g, uint16_t *e16,
                                               uint8_t *codes, float *scales,
                                               int64_t N, int R, int G, int B,
                                               float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     int64_t S = N / R;
     float omb = 1.0f - beta;
-    float c[8192];
-    int8_t q[8192];
+    float c[ORC_MAX_BLOCK];
+    int8_t q[ORC_MAX_BLOCK];
     for (int64_t slice = 0; slice < R; ++slice) {
         int64_t p = orc_send_position(slice, R, G);
         for (int64_t b0 = 0; b0 < S; b0 += B) {
@@ -285,18 +304,21 @@ ORC_EXPORT void orc_ef_quant_int4_rank_bf16ef(const uint16_t *g, uint16_t *e16,
             }
         }
     }
+    return 0;
 }
 
-ORC_EXPORT void orc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *e16,
+ORC_EXPORT int orc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *e16,
                                          uint8_t *codes, float *scales,
                                          int64_t N, int R, int G, int B,
                                          float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     for (int r = 0; r < R; ++r)
         orc_ef_quant_int4_rank_bf16ef(g + (int64_t)r * N, e16 + (int64_t)r * N,
                                       codes + (int64_t)r * (N / 2),
                                       scales + (int64_t)r * (N / B),
                                       N, R, G, B, s, beta);
+    return 0;
 }
 
 /*
@@ -310,17 +332,18 @@ ORC_EXPORT void orc_ef_quant_int4_bf16ef(const uint16_t *g, uint16_t *e16,
  * orc_ef_quant_int4_rank.  e8: N codes and e8s: N/B scales of one rank, in
  * place (a zero buffer is all-zero codes and scales).
  */
-ORC_EXPORT void orc_ef_quant_int4_rank_int8ef(const uint16_t *g, int8_t *e8, float *e8s,
+ORC_EXPORT int orc_ef_quant_int4_rank_int8ef(const uint16_t *g, int8_t *e8, float *e8s,
                                               uint8_t *codes, float *scales,
                                               int64_t N, int R, int G, int B,
                                               float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     int64_t S = N / R;
     float one_mb = 1.0f - beta;
-    float c8[8192];
-    float ev8[8192];
-    float en8[8192];
-    int8_t q8[8192];
+    float c8[ORC_MAX_BLOCK];
+    float ev8[ORC_MAX_BLOCK];
+    float en8[ORC_MAX_BLOCK];
+    int8_t q8[ORC_MAX_BLOCK];
     for (int64_t slice = 0; slice < R; ++slice) {
         int64_t p = orc_send_position(slice, R, G);
         for (int64_t b0 = 0; b0 < S; b0 += B) {
@@ -348,19 +371,22 @@ ORC_EXPORT void orc_ef_quant_int4_rank_int8ef(const uint16_t *g, int8_t *e8, flo
             orc_quant_block(en8, B, 127, e8 + in0, &e8s[in0 / B]);
         }
     }
+    return 0;
 }
 
-ORC_EXPORT void orc_ef_quant_int4_int8ef(const uint16_t *g, int8_t *e8, float *e8s,
+ORC_EXPORT int orc_ef_quant_int4_int8ef(const uint16_t *g, int8_t *e8, float *e8s,
                                          uint8_t *codes, float *scales,
                                          int64_t N, int R, int G, int B,
                                          float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     for (int r = 0; r < R; ++r)
         orc_ef_quant_int4_rank_int8ef(g + (int64_t)r * N, e8 + (int64_t)r * N,
                                       e8s + (int64_t)r * (N / B),
                                       codes + (int64_t)r * (N / 2),
                                       scales + (int64_t)r * (N / B),
                                       N, R, G, B, s, beta);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -387,15 +413,35 @@ static float dq_at(const uint8_t *codes, const float *scales, int64_t pos, int B
  *   k = g*L + l adds sub-slice g of units (0, l), (1, l), ..., (G-1, l).
  * In both cases out holds S values.
  */
+ORC_EXPORT void orc_dequant_reduce_dest_range(const uint8_t *codes,
+                                              const float *scales,
+                                              int64_t N, int R, int G, int B, int k,
+                                              int64_t i0, int64_t i1,
+                                              float out_scale, void *out,
+                                              int out_bf16);
+
 ORC_EXPORT void orc_dequant_reduce_dest(const uint8_t *codes,
                                         const float *scales,
                                         int64_t N, int R, int G, int B, int k,
                                         float out_scale, void *out,
                                         int out_bf16)
 {
+    orc_dequant_reduce_dest_range(codes, scales, N, R, G, B, k, 0, N / R,
+                                  out_scale, out, out_bf16);
+}
+
+/* Outputs [i0, i1) of destination k, written to out[0 .. i1-i0): every
+ * output is its own sum, so a range is exactly that part of the whole. */
+ORC_EXPORT void orc_dequant_reduce_dest_range(const uint8_t *codes,
+                                              const float *scales,
+                                              int64_t N, int R, int G, int B, int k,
+                                              int64_t i0, int64_t i1,
+                                              float out_scale, void *out,
+                                              int out_bf16)
+{
     int64_t S = N / R;
     int L = R / G;
-    for (int64_t i = 0; i < S; ++i) {
+    for (int64_t i = i0; i < i1; ++i) {
         float acc = 0.0f;
         if (G == 1) {
             for (int r = 0; r < R; ++r) {
@@ -411,8 +457,8 @@ ORC_EXPORT void orc_dequant_reduce_dest(const uint8_t *codes,
             }
         }
         float v = acc * out_scale;
-        if (out_bf16) ((uint16_t *)out)[i] = orc_f32_to_bf16_rne(v);
-        else          ((float *)out)[i] = v;
+        if (out_bf16) ((uint16_t *)out)[i - i0] = orc_f32_to_bf16_rne(v);
+        else          ((float *)out)[i - i0] = v;
     }
 }
 
@@ -442,7 +488,7 @@ ORC_EXPORT void orc_dequant_reduce(const uint8_t *codes, const float *scales,
  * error feedback on this hop.  Output: G*S codes (G*S/2 bytes) and G*S/B
  * scales, sub-slice g' first-to-last; sub-slice g' is bound for rank g'*L + l.
  */
-ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
+ORC_EXPORT int orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
                                                    const float *scales,
                                                    int64_t N, int R, int G, int B,
                                                    int g, int l,
@@ -450,15 +496,15 @@ ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
                                                    float *out_scales,
                                                    float *e1, float s, float beta);
 
-ORC_EXPORT void orc_dequant_reduce_requant_unit(const uint8_t *codes,
+ORC_EXPORT int orc_dequant_reduce_requant_unit(const uint8_t *codes,
                                                 const float *scales,
                                                 int64_t N, int R, int G, int B,
                                                 int g, int l,
                                                 uint8_t *out_codes,
                                                 float *out_scales)
 {
-    orc_dequant_reduce_requant_unit_ef(codes, scales, N, R, G, B, g, l,
-                                       out_codes, out_scales, 0, 0.0f, 0.0f);
+    return orc_dequant_reduce_requant_unit_ef(codes, scales, N, R, G, B, g, l,
+                                              out_codes, out_scales, 0, 0.0f, 0.0f);
 }
 
 /*
@@ -470,7 +516,7 @@ ORC_EXPORT void orc_dequant_reduce_requant_unit(const uint8_t *codes,
  *   c = p + s * e1;  q, scale = Q4(c);  e1 <- beta * e1 + (1 - beta) * (c - d).
  * e1 == NULL is the plain first hop.
  */
-ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
+ORC_EXPORT int orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
                                                    const float *scales,
                                                    int64_t N, int R, int G, int B,
                                                    int g, int l,
@@ -478,11 +524,12 @@ ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
                                                    float *out_scales,
                                                    float *e1, float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     int64_t S = N / R;
     int L = R / G;
     float one_minus_beta = 1.0f - beta;
-    float part[8192];
-    int8_t q[8192];
+    float part[ORC_MAX_BLOCK];
+    int8_t q[ORC_MAX_BLOCK];
     for (int gq = 0; gq < G; ++gq) {
         for (int64_t b0 = 0; b0 < S; b0 += B) {
             int64_t out0 = (int64_t)gq * S + b0;
@@ -515,17 +562,19 @@ ORC_EXPORT void orc_dequant_reduce_requant_unit_ef(const uint8_t *codes,
             }
         }
     }
+    return 0;
 }
 
 /* Every unit: out_codes is [R][G*S/2], out_scales [R][G*S/B], unit g*L + l;
  * e1 (or NULL) is [R][G*S] in the same unit order. */
-ORC_EXPORT void orc_dequant_reduce_requant_ef(const uint8_t *codes,
+ORC_EXPORT int orc_dequant_reduce_requant_ef(const uint8_t *codes,
                                               const float *scales,
                                               int64_t N, int R, int G, int B,
                                               uint8_t *out_codes,
                                               float *out_scales,
                                               float *e1, float s, float beta)
 {
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
     int64_t S = N / R;
     int L = R / G;
     for (int g = 0; g < G; ++g)
@@ -537,16 +586,17 @@ ORC_EXPORT void orc_dequant_reduce_requant_ef(const uint8_t *codes,
                                                e1 ? e1 + unit * (G * S) : 0,
                                                s, beta);
         }
+    return 0;
 }
 
-ORC_EXPORT void orc_dequant_reduce_requant(const uint8_t *codes,
+ORC_EXPORT int orc_dequant_reduce_requant(const uint8_t *codes,
                                            const float *scales,
                                            int64_t N, int R, int G, int B,
                                            uint8_t *out_codes,
                                            float *out_scales)
 {
-    orc_dequant_reduce_requant_ef(codes, scales, N, R, G, B, out_codes,
-                                  out_scales, 0, 0.0f, 0.0f);
+    return orc_dequant_reduce_requant_ef(codes, scales, N, R, G, B, out_codes,
+                                         out_scales, 0, 0.0f, 0.0f);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -554,14 +604,16 @@ ORC_EXPORT void orc_dequant_reduce_requant(const uint8_t *codes,
 /* ------------------------------------------------------------------------ */
 
 /* [qwZ]: per block of B weights, symmetric int8 with scale absmax / 127. */
-ORC_EXPORT void orc_qwz_quant_int8(const uint16_t *w, int8_t *codes,
+ORC_EXPORT int orc_qwz_quant_int8(const uint16_t *w, int8_t *codes,
                                    float *scales, int64_t n, int B)
 {
-    float x[8192];
+    if (!orc_block_ok(B)) return ORC_EBLOCK;
+    float x[ORC_MAX_BLOCK];
     for (int64_t b0 = 0; b0 < n; b0 += B) {
         for (int i = 0; i < B; ++i) x[i] = orc_bf16_to_f32(w[b0 + i]);
         orc_quant_block(x, B, 127, codes + b0, &scales[b0 / B]);
     }
+    return 0;
 }
 
 /* Back to bf16: code times scale (one rounding), then rounded to bf16. */
@@ -576,12 +628,13 @@ ORC_EXPORT void orc_qwz_dequant_int8(const int8_t *codes, const float *scales,
  * the copy a node keeps after the forward all-gather (the hierarchical
  * partition of "ZeROPlusPlus.md" §1.2 keeps a full model copy in each node).
  * Exactly orc_qwz_quant_int8 followed by orc_qwz_dequant_int8. */
-ORC_EXPORT void orc_qwz_quant_replica_int8(const uint16_t *w, int8_t *codes,
+ORC_EXPORT int orc_qwz_quant_replica_int8(const uint16_t *w, int8_t *codes,
                                            float *scales, uint16_t *replica,
                                            int64_t n, int B)
 {
-    orc_qwz_quant_int8(w, codes, scales, n, B);
+    if (orc_qwz_quant_int8(w, codes, scales, n, B) != 0) return ORC_EBLOCK;
     orc_qwz_dequant_int8(codes, scales, replica, n, B);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -240,6 +240,28 @@ def test_reduce_of_one_rank_is_dequantization(orc):
     assert np.array_equal(out.view(np.uint32), d.view(np.uint32))
 
 
+@pytest.mark.parametrize("G,out_bf16", [(1, False), (2, True)])
+def test_destination_ranges_tile_the_destination(orc, G, out_bf16):
+    """Every output is its own sum, so the outputs [i0, i1) of a destination
+    are exactly that part of the destination's result, for any split -- the
+    all-cores CPU baseline relies on this."""
+    R, N, B = 4, 4 * 6 * 64, 64
+    g = wl.as_u16(wl.draw_bf16(R * N, 1e-3, 7)).copy()
+    codes, scales = orc.ef_quant_int4(g, None, N, R, G, B, 1.0, 0.0)
+    if G > 1:
+        codes, scales = orc.dequant_reduce_requant(codes, scales, N, R, G, B)
+    S = N // R
+    for k in range(R):
+        whole = orc.dequant_reduce_dest(codes, scales, N, R, G, B, k, 0.5, out_bf16)
+        for cuts in ([0, S], [0, 64, S], [0, 0, 128, 320, S]):
+            parts = [orc.dequant_reduce_dest_range(codes, scales, N, R, G, B, k, a, b, 0.5, out_bf16)
+                     for a, b in zip(cuts[:-1], cuts[1:])]
+            got = np.concatenate(parts)
+            assert got.dtype == whole.dtype and np.array_equal(got.view(np.uint8), whole.view(np.uint8))
+    with pytest.raises(ValueError):
+        orc.dequant_reduce_dest_range(codes, scales, N, R, G, B, 0, 10, 5)
+
+
 def test_identical_ranks_sum_to_r_times_d(orc):
     R, N, B = 8, 8 * 512, 256
     one = wl.as_u16(wl.draw_bf16(N, 1e-3, 11)).copy()
