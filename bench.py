@@ -760,44 +760,72 @@ def oracle_qgz_step(orc, w: wl.QgzWorkload, g_u16: np.ndarray, ef: np.ndarray):
     return orc.dequant_reduce(codes, scales, w.N, w.R, 1, w.B, 1.0, w.out_bf16)
 
 
-def oracle_qgz_step_threaded(orc, w: wl.QgzWorkload, g_u16: np.ndarray, ef: np.ndarray, pool):
-    """The same step with the oracle's independent pieces -- one rank's
-    quantization, one first-hop unit, one destination's reduce -- run on a
-    thread pool (the oracle's C calls release the interpreter lock)."""
+def oracle_qgz_step_threaded(orc, w: wl.QgzWorkload, g_u16: np.ndarray, ef: np.ndarray, pool,
+                             pieces: int = 1):
+    """The same step with the oracle's independent pieces run on a thread
+    pool (the oracle's C calls release the interpreter lock):
+      * quantization by (rank, slice): every block lies in one slice, so a
+        slice is quantized as a one-rank problem of S elements and its codes
+        and scales are placed at the slice's send position;
+      * the first hop by unit;
+      * each destination's reduce in `pieces` block-aligned output ranges
+        (every output is its own sum)."""
     N, R, G, B = w.N, w.R, w.G, w.B
-    parts = list(pool.map(lambda r: orc.ef_quant_int4_rank(
-        g_u16[r * N:(r + 1) * N], ef[r * N:(r + 1) * N], N, R, G, B, w.err_scale, w.err_beta),
-        range(R)))
-    codes = np.concatenate([p[0] for p in parts])
-    scales = np.concatenate([p[1] for p in parts])
+    S = N // R
+    codes = np.empty(R * N // 2, np.uint8)
+    scales = np.empty(R * N // B, np.float32)
+
+    def quant(item):
+        r, k = divmod(item, R)
+        x0 = r * N + k * S
+        c, sc = orc.ef_quant_int4_rank(g_u16[x0:x0 + S], ef[x0:x0 + S], S, 1, 1, B,
+                                       w.err_scale, w.err_beta)
+        y0 = r * N + orc.send_position(k, R, G) * S
+        codes[y0 // 2:(y0 + S) // 2] = c
+        scales[y0 // B:(y0 + S) // B] = sc
+
+    list(pool.map(quant, range(R * R)))
     if G > 1:
         L = R // G
         units = list(pool.map(lambda u: orc.dequant_reduce_requant_unit(
             codes, scales, N, R, G, B, u // L, u % L), range(R)))
         codes = np.concatenate([u[0] for u in units])
         scales = np.concatenate([u[1] for u in units])
-    shards = list(pool.map(lambda k: orc.dequant_reduce_dest(
-        codes, scales, N, R, G, B, k, 1.0, w.out_bf16), range(R)))
-    return np.concatenate(shards)
+    out = np.empty(N, np.uint16 if w.out_bf16 else np.float32)
+    blocks = S // B
+    bounds = [B * (blocks * j // pieces) for j in range(pieces + 1)]
+
+    def reduce(item):
+        k, j = divmod(item, pieces)
+        i0, i1 = bounds[j], bounds[j + 1]
+        out[k * S + i0:k * S + i1] = orc.dequant_reduce_dest_range(
+            codes, scales, N, R, G, B, k, i0, i1, 1.0, w.out_bf16)
+
+    list(pool.map(reduce, range(R * pieces)))
+    return out
 
 
 def cpu_baseline_qgz_threaded(w: wl.QgzWorkload, steps: int, fraction: int, g_u16: np.ndarray):
-    """The oracle on all host cores: ranks, first-hop units and destinations
-    spread over a thread pool of min(R, cores) threads."""
+    """The oracle on all host cores: the pieces of oracle_qgz_step_threaded
+    spread over one thread per core."""
     from concurrent.futures import ThreadPoolExecutor
     import oracle
     orc = oracle.get()
     sw = qgz_sample(w, fraction)
     cores, _ = host_cpu()
-    threads = max(1, min(sw.R, cores))
+    threads = max(1, cores)
+    pieces = max(1, -(-2 * threads // sw.R))  # at least two reduce pieces per thread
     ef = np.zeros(sw.R * sw.N, np.float32)
     with ThreadPoolExecutor(threads) as pool:
         t0 = time.perf_counter()
         for _ in range(steps):
-            oracle_qgz_step_threaded(orc, sw, g_u16, ef, pool)
+            oracle_qgz_step_threaded(orc, sw, g_u16, ef, pool, pieces)
         dt = time.perf_counter() - t0
     return {"value": sw.R * sw.N * steps / dt, "unit": "elements/s", "cores": threads,
-            "kind": "oracle", "sample": f"the same {steps} steps, {dt:.1f} s on {threads} threads"}
+            "kind": "oracle",
+            "sample": f"the same {steps} steps, {dt:.1f} s on {threads} threads "
+                      f"(quantization by rank and slice, first hop by unit, each "
+                      f"destination's reduce in {pieces} ranges)"}
 
 
 def gpu_parity_on_sample(sw: wl.QgzWorkload, g_u16: np.ndarray, steps: int,

@@ -97,9 +97,10 @@ def test_cpulist_parser():
 
 @pytest.mark.parametrize("name", ["qgz_tiny", "qgz_hierarchical"])
 def test_threaded_oracle_step_matches_the_plain_step(name):
-    """The all-cores CPU baseline runs the oracle's per-rank, per-unit and
-    per-destination calls on threads; it must compute the same bits (and
-    leave the same error buffer) as the oracle's whole-step calls."""
+    """The all-cores CPU baseline runs the oracle's per-slice quantization,
+    per-unit first hop and ranged destination reduces on threads; it must
+    compute the same bits (and leave the same error buffer) as the oracle's
+    whole-step calls."""
     from concurrent.futures import ThreadPoolExecutor
     import numpy as np
     import oracle
@@ -110,9 +111,9 @@ def test_threaded_oracle_step_matches_the_plain_step(name):
     ef_a = np.zeros(w.R * w.N, np.float32)
     ef_b = np.zeros(w.R * w.N, np.float32)
     with ThreadPoolExecutor(4) as pool:
-        for _ in range(2):
+        for pieces in (1, 3):
             a = bench.oracle_qgz_step(orc, w, g, ef_a)
-            b = bench.oracle_qgz_step_threaded(orc, w, g, ef_b, pool)
+            b = bench.oracle_qgz_step_threaded(orc, w, g, ef_b, pool, pieces)
             assert a.dtype == b.dtype and np.array_equal(a.view(np.uint8), b.view(np.uint8))
             assert np.array_equal(ef_a.view(np.uint32), ef_b.view(np.uint32))
 
