@@ -682,7 +682,8 @@ def run_qwz(w: wl.QwzWorkload, args, dev, dist, ws):
                          "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
                          "frac": kernels["qwz_quant_int8"]["frac"],
                          "traffic": ncu_traffic("qwz_quant_int8", "qwz", w.n)},
-            "kernels": kernels, "gpu_launches": 2 * args.steps, "clocks": clocks}, None
+            "kernels": kernels, "gpu_launches": 2 * args.steps, "clocks": clocks}, \
+        (wd, codes, scales, back, stream)
 
 
 def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
@@ -737,7 +738,123 @@ def run_sr(w: wl.SrWorkload, args, dev, dist, ws):
                                           "algorithmic_bytes": b,
                                           "GB/s": round(achieved, 1),
                                           "frac": round(achieved / peak, 4)}},
-            "gpu_launches": w.micro_steps * args.steps, "clocks": clocks}, None
+            "gpu_launches": w.micro_steps * args.steps, "clocks": clocks}, \
+        (dst, srcs, pristine, stream)
+
+
+# ---------------------------------------------------------------------------
+# the other configurations, summarized on the default line
+# ---------------------------------------------------------------------------
+
+def qgz_parity_on_sample(w: wl.QgzWorkload, fraction: int, steps: int, dev) -> dict:
+    """`steps` chained steps of a 1/fraction sample of w, oracle against the
+    CUDA path (every shard and error-buffer element)."""
+    import oracle
+    orc = oracle.get()
+    sw = qgz_sample(w, fraction)
+    g = wl.as_u16(wl.qgz_gradients(sw, 0)).ravel().copy()
+    ef = np.zeros(sw.R * sw.N, np.float32)
+    for _ in range(steps):
+        out = oracle_qgz_step(orc, sw, g, ef)
+    return gpu_parity_on_sample(sw, g, steps, out, ef, dev)
+
+
+def qwz_parity(w: wl.QwzWorkload, tensors, dev) -> dict:
+    """Sampled block ranges (the first and the last 2^20 weights) of the
+    full-size qwZ run against the oracle: the one-pass replica kernel's codes,
+    scales and bf16 replica, then the dequant kernel's bf16 weights."""
+    import oracle
+    from weight_communication_gb300 import binding
+    orc = oracle.get()
+    wd, codes, scales, back, stream = tensors
+    m = min(w.n, 1 << 20) // w.B * w.B
+    ranges = [(0, m), (w.n - m, w.n)]
+    with torch.cuda.stream(stream):
+        binding.qwz_quant_replica_int8(wd, codes, scales, back, w.B, stream)
+        torch.cuda.synchronize(dev)
+        rep = [back[a:b].clone() for a, b in ranges]
+        binding.qwz_dequant_int8(codes, scales, back, w.B, stream)
+        torch.cuda.synchronize(dev)
+    ok = True
+    for (a, b), r in zip(ranges, rep):
+        wc, ws_, wr = orc.qwz_quant_replica_int8(wl.as_u16(wd[a:b]).copy(), w.B)
+        ok &= np.array_equal(codes[a:b].cpu().numpy(), wc)
+        ok &= np.array_equal(scales[a // w.B:b // w.B].cpu().numpy().view(np.uint32), ws_.view(np.uint32))
+        ok &= np.array_equal(wl.as_u16(r), wr)
+        ok &= np.array_equal(wl.as_u16(back[a:b]), orc.qwz_dequant_int8(wc, ws_, w.B))
+    return {"verdict": "bit-exact" if ok else "MISMATCH",
+            "compared": f"codes, scales, replica and dequantized weights of the first and last "
+                        f"{m} weights of the full-size run, against the oracle"}
+
+
+def sr_parity(w: wl.SrWorkload, tensors, dev) -> dict:
+    """One more full-size launch (micro-step 0) from the timed run's state;
+    its first 2^22 outputs and zeroed sources against the oracle."""
+    import oracle
+    from weight_communication_gb300 import binding
+    orc = oracle.get()
+    dst, srcs, pristine, stream = tensors
+    m = min(w.n, 1 << 22)
+    with torch.cuda.stream(stream):
+        srcs[0].copy_(pristine[0])
+        torch.cuda.synchronize(dev)
+        d0 = wl.as_u16(dst[:m]).copy()
+        s0 = wl.as_u16(srcs[0][:m]).copy()
+        binding.sr_accumulate_bf16(dst, srcs[0], w.seed, 0, stream)
+        torch.cuda.synchronize(dev)
+    orc.sr_accumulate_bf16(d0, s0, w.seed, 0)
+    ok = np.array_equal(wl.as_u16(dst[:m]), d0) and np.array_equal(wl.as_u16(srcs[0][:m]), s0)
+    return {"verdict": "bit-exact" if ok else "MISMATCH",
+            "compared": f"the first {m} outputs and zeroed sources of one full-size launch "
+                        f"(seed {w.seed}, micro-step 0), against the oracle"}
+
+
+def other_workloads(args, dev, dist, ws, rank) -> dict:
+    """The hierarchical two-hop step, qwZ and the SR accumulate at full size,
+    plus the single-hop step's low-precision error buffers and fused form:
+    per kernel the mean and median event time, algorithmic bytes and fraction
+    of the HBM peak, over at most 20 timed steps each.  With the CPU legs on
+    (rank 0 of a single process), the first three also carry a parity verdict
+    from a sample through the CUDA path against the oracle."""
+    sub = argparse.Namespace(**vars(args))
+    sub.steps = max(1, min(args.steps, 20))
+    sub.warmup = 3
+    sub.no_e2e = True
+    sub.no_overlap = True
+    check = rank == 0 and ws == 1 and not args.no_cpu_baseline
+
+    def entry(line, parity=None):
+        e = {"workload": line["config"]["workload"], "steps": sub.steps,
+             "ms_per_step": round(line["ms_per_step"], 5), "kernels": line["kernels"],
+             "clocks": line["clocks"]}
+        if parity is not None:
+            e["parity"] = parity
+        return e
+
+    out = {}
+    line, _ = run_qgz(wl.QGZ_HIERARCHICAL, sub, dev, dist, ws)
+    out["qgz_hierarchical"] = entry(
+        line, qgz_parity_on_sample(wl.QGZ_HIERARCHICAL, 64, 2, dev) if check else None)
+    torch.cuda.empty_cache()
+    line, _ = run_qgz(wl.QGZ_HIERARCHICAL, sub, dev, dist, ws, hop1_ef=True)
+    out["qgz_hier_ef"] = entry(line)
+    torch.cuda.empty_cache()
+    for ef in ("bf16", "int8"):
+        line, _ = run_qgz(wl.QGZ_SINGLE_HOP, sub, dev, dist, ws, ef=ef)
+        out[f"qgz_{ef}ef"] = entry(line)
+        torch.cuda.empty_cache()
+    line, _ = run_qgz_fused(wl.QGZ_SINGLE_HOP, sub, dev, dist, ws)
+    out["qgz_fused"] = entry(line)
+    torch.cuda.empty_cache()
+    line, t = run_qwz(wl.QWZ_WEIGHTS, sub, dev, dist, ws)
+    out["qwz"] = entry(line, qwz_parity(wl.QWZ_WEIGHTS, t, dev) if check else None)
+    del t
+    torch.cuda.empty_cache()
+    line, t = run_sr(wl.SR_ACCUMULATE, sub, dev, dist, ws)
+    out["sr"] = entry(line, sr_parity(wl.SR_ACCUMULATE, t, dev) if check else None)
+    del t
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -938,6 +1055,8 @@ def main(argv=None):
     ap.add_argument("--no-overlap", action="store_true",
                     help="skip the extra pass that overlaps each reduce with the next EF-quant")
     ap.add_argument("--no-clocks", dest="clocks", action="store_false")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the summary of the other configurations on the default line")
     ap.add_argument("--scale", type=int, default=1,
                     help="divide each rank's gradient by this (profiling a smaller case)")
     ap.add_argument("--batches", type=int, default=4,
@@ -985,6 +1104,9 @@ def main(argv=None):
                 line["cpu_baseline"] = cpu_baseline_qgz(w, 20, fraction, g_example.cpu(), dev)
                 line["parity"] = line["cpu_baseline"].pop("parity")
             del g_example
+            if name == "qgz_single_hop" and args.scale == 1 and not args.no_workloads:
+                torch.cuda.empty_cache()
+                line["workloads"] = other_workloads(args, dev, dist, ws, rank)
         elif name == "qwz":
             qw = wl.QWZ_WEIGHTS
             if args.scale > 1:

@@ -14,18 +14,23 @@
 // Output element o (over all R units, G*S each) belongs to unit u = g*L + l,
 // sub-slice g' and offset i; its inputs are the codes at position
 // (g*L + l')*N + (l*G + g')*S + i for l' = 0..L-1.  Per output the kernel
-// reads L codes and scales (L/2 + 4L/B bytes) and writes half a byte: at L = 8
-// it does about 40 fp32/int operations per 4.6 bytes, so it is issue-bound,
-// and the work goes into keeping the instruction count per code at its floor
-// (one byte permute and three exact fp32 operations, two for the first
-// source, whose add to the +0 start folds into one fma).
+// reads L codes and scales (L/2 + 4L/B bytes) and writes half a byte, so it
+// is bound by instruction issue, not bytes, and the work goes into the
+// instructions per code.
 //
 // Fast path (B = 256, 512, 1024 and L a power of two up to 16): one warp per
 // output block, lane t owning outputs t*B/32 .. t*B/32 + B/32 - 1, the source
 // count a template parameter so that all L loads are issued before the adds,
 // and a 3-D grid (block, sub-slice, unit) that spares the index divisions.
-// Other shapes: a general kernel (lane groups of 8 consecutive outputs,
-// sources fetched 8 at a time).
+// The warp's outputs are one block of every source, so a source's codes take
+// only 16 distinct products: each lane forms one of them, and a code's
+// product is fetched by one shuffle indexed by its nibble (product_table in
+// wc_device.cuh) -- a shift, a shuffle and half a packed add per code, in
+// place of an unpack, an unbias, a multiply and an add.  The shuffles run on
+// the load/store pipe, so the last source takes the byte-permute path, in
+// packed form, on the ALU and FMA pipes.  The requantization is packed as
+// well (requantize_pairs).  Other shapes: a general kernel (lane groups of 8
+// consecutive outputs, sources fetched 8 at a time, scalar arithmetic).
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
@@ -139,6 +144,76 @@ __device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, bool out
     if (out_ok && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
 }
 
+// requantize_lane on the E values of a lane held as E/2 packed pairs (p[j]:
+// values 2j, 2j+1), in packed exact arithmetic, with the codes packed through
+// the biased rounding of kRoundShift4: the same codes, scale and error
+// update bit for bit.  The whole warp holds one block (LPB = 32).
+template <int E, bool HAS_EF, int B>
+__device__ __forceinline__ void requantize_pairs(f32x2 p[E / 2], uint32_t o, bool out_ok, int lane,
+                                                 uint8_t *__restrict__ out_codes,
+                                                 float *__restrict__ out_scales,
+                                                 float *__restrict__ ef1, float s, float beta,
+                                                 float one_minus_beta, const Ops2 &ops) {
+    f32x2 e[HAS_EF ? E / 2 : 1];
+    if (HAS_EF) {
+        const f32x2 s2 = pack2(s, s);
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+            const float4 v = out_ok ? ld_stream_f4(ef1 + o + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            e[2 * q] = pack2(v.x, v.y);
+            e[2 * q + 1] = pack2(v.z, v.w);
+        }
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j) p[j] = ops.add(p[j], ops.mul(s2, e[HAS_EF ? j : 0]));
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j) {
+        float a, b;
+        unpack2(p[j], a, b);
+        m = max3(m, fabsf(a), fabsf(b));
+    }
+    m = group_max<kWarp>(m);
+    const BlockScale bs = block_scale<7>(m);
+    const f32x2 inv2 = pack2(bs.inv, bs.inv), sc2 = pack2(bs.scale, bs.scale);
+    const f32x2 shift = pack2(kRoundShift4, kRoundShift4), unshift = pack2(-kRoundShift4, -kRoundShift4);
+    const f32x2 beta2 = pack2(beta, beta), omb2 = pack2(one_minus_beta, one_minus_beta);
+    uint32_t words[E / 8];
+#pragma unroll
+    for (int wq = 0; wq < E / 8; ++wq) {
+        uint32_t pairs[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * wq + jj;
+            const f32x2 r = ops.add(ops.mul(p[j], inv2), shift);
+            float r0, r1;
+            unpack2(r, r0, r1);
+            pairs[jj] = __float_as_uint(r0) + (__float_as_uint(r1) << 4);
+            if (HAS_EF) {
+                const f32x2 d = ops.mul(ops.add(r, unshift), sc2);  // the code (exact) * scale
+                p[j] = ops.add(ops.mul(beta2, e[HAS_EF ? j : 0]), ops.mul(omb2, ops.sub(p[j], d)));
+            }
+        }
+        words[wq] = pack_int4_pairs(pairs);
+    }
+    if (out_ok) store_words<E / 8>(out_codes + o / 2, words);
+    if (HAS_EF && out_ok) {
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+            float a, b, c, d;
+            unpack2(p[2 * q], a, b);
+            unpack2(p[2 * q + 1], c, d);
+            __stcs(reinterpret_cast<float4 *>(ef1 + o + 4 * q), make_float4(a, b, c, d));
+        }
+    }
+    if (out_ok && lane == 0) __stcs(out_scales + o / B, bs.scale);
+}
+
+// Sources of the fixed kernel that read their products from a table (the
+// lookups run on the load/store pipe; the last source takes the packed
+// byte-permute path on the ALU and FMA pipes instead).
+__host__ __device__ constexpr int hop1_table_sources(int L) { return L - (L + 7) / 8; }
+
 // Launch bounds: a budget for 5 CTAs per SM (at most 51 registers) at B <= 512
 // measured faster than the compiler's unbounded choice -- at B = 512, L = 8,
 // 0.594 -> 0.574 ms without error feedback (48 registers instead of 40) and
@@ -150,7 +225,7 @@ __global__ void __launch_bounds__(256, B <= 512 ? 5 : 1)
 hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                   uint8_t *__restrict__ out_codes, float *__restrict__ out_scales,
                   QgzGeometry geo, float *__restrict__ ef1, float s, float beta,
-                  float one_minus_beta) {
+                  float one_minus_beta, Exact2 kc) {
     constexpr int E = B / kWarp;  // outputs per lane
     constexpr int W = E / 8;      // code words per lane and source
     const int lane = threadIdx.x & (kWarp - 1);
@@ -181,22 +256,29 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
             sc[t] = __ldg(sp + size_t(t) * sstride);
         }
     }
-    float p[E];
+    // The warp's E * 32 outputs are one block of every source, so each
+    // source's products come from one warp-wide table.
+    constexpr int NT = hop1_table_sources(L);
+    const Ops2 ops(kc);
+    f32x2 p[E / 2];
 #pragma unroll
     for (int t = 0; t < L; ++t) {
+        const f32x2 s2 = pack2(sc[t], sc[t]);
+        const float table = t >= NT ? 0.0f
+                            : t == 0 ? product_table<true>(sc[t], lane)
+                                     : product_table<false>(sc[t], lane);
 #pragma unroll
         for (int wq = 0; wq < W; ++wq) {
-            float f[8];
-            unpack_int4x8(w[t][wq], f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                p[8 * wq + j] = t == 0 ? dequant_first(f[j], sc[t])
-                                       : __fadd_rn(p[8 * wq + j], dequant(f[j], sc[t]));
+            f32x2 *pw = p + 4 * wq;
+            if (t == 0 && t < NT) accumulate_word<true, true, kWarp>(w[t][wq], table, s2, pw, kFull, ops);
+            else if (t == 0) accumulate_word<true, false, kWarp>(w[t][wq], table, s2, pw, kFull, ops);
+            else if (t < NT) accumulate_word<false, true, kWarp>(w[t][wq], table, s2, pw, kFull, ops);
+            else accumulate_word<false, false, kWarp>(w[t][wq], table, s2, pw, kFull, ops);
         }
     }
     const bool out_ok = WC_IN_BOUNDS(uint64_t(o) + E <= uint64_t(geo.G) * geo.N);
-    requantize_lane<E, kWarp, HAS_EF, B>(p, o, out_ok, lane, out_codes, out_scales, ef1, s, beta,
-                                         one_minus_beta);
+    requantize_pairs<E, HAS_EF, B>(p, o, out_ok, lane, out_codes, out_scales, ef1, s, beta,
+                                   one_minus_beta, ops);
 }
 
 // General shapes: warp tile T = max(B, 256) outputs, lane t holds outputs
@@ -314,18 +396,19 @@ static bool launch_fixed_b(const uint8_t *codes, const float *scales, uint8_t *o
     const uint32_t warps = geo.S / B;  // per sub-slice
     const dim3 grid((warps + 7) / 8, geo.G, geo.R);
     const float omb = 1.0f - beta;
+    const Exact2 kc = exact2_constants();
 #define WC_HOP1(LL)                                                                           \
     case LL:                                                                                  \
         hop1_fixed_kernel<B, LL, HAS_EF><<<grid, 256, 0, stream>>>(codes, scales, out_codes,  \
                                                                    out_scales, geo, ef1, s,   \
-                                                                   beta, omb);                \
+                                                                   beta, omb, kc);            \
         return true;
     switch (geo.L) {
         WC_HOP1(1) WC_HOP1(2) WC_HOP1(4) WC_HOP1(8)
         case 16:
             if (B > 512) return false;  // 16 sources x 4 words would not fit in registers
             hop1_fixed_kernel<B, (B > 512 ? 8 : 16), HAS_EF><<<grid, 256, 0, stream>>>(
-                codes, scales, out_codes, out_scales, geo, ef1, s, beta, omb);
+                codes, scales, out_codes, out_scales, geo, ef1, s, beta, omb, kc);
             return true;
         default:
             return false;

@@ -38,6 +38,121 @@ namespace wc {
 // kept in registers until a second warp reduction has found its maximum).
 enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2, kEfInt8 = 3 };
 
+// The int8 error buffer's step for whole-warp blocks (B >= 128), in packed
+// exact arithmetic (wc_device.cuh): the same operations as the EF = kEfInt8
+// case of ef_quant_int4_warp, two elements per instruction, with the codes of
+// both quantizations packed through biased rounding (q + 8 and q + 128 in the
+// low byte).  Every code, scale and stored error is the one the scalar chain
+// gives, bit for bit.  Lane t holds elements 128k + 4t + j as pairs
+// (j = 0, 1) and (2, 3).
+template <int B>
+__device__ __forceinline__ void ef_quant_int8ef_pairs(const uint16_t *__restrict__ g,
+                                                      int8_t *__restrict__ ef8,
+                                                      float *__restrict__ ef_scales,
+                                                      uint8_t *__restrict__ codes,
+                                                      float *__restrict__ scales, QgzGeometry geo,
+                                                      float s, float beta, float one_minus_beta,
+                                                      const Exact2 &kc) {
+    static_assert(B >= 128 && B % 128 == 0, "one warp per block");
+    constexpr int K = B / 128;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const uint32_t off = (blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp) * B;
+    if (off >= geo.S) return;  // whole warp
+    const uint32_t slice = blockIdx.y, r = blockIdx.z;
+    uint32_t p = slice;
+    if (geo.G > 1) {
+        const uint32_t gq = slice / geo.L;
+        p = (slice - gq * geo.L) * geo.G + gq;
+    }
+    const uint32_t tile0 = r * geo.N + slice * geo.S + off;
+    const uint32_t out0 = r * geo.N + p * geo.S + off;
+    const uint32_t eblk = tile0 / B;
+    const Ops2 ops(kc);
+
+    float es = 0.0f;
+    if (WC_IN_BOUNDS(eblk < geo.total / B)) es = __ldg(ef_scales + eblk);
+    uint2 gv[K];
+    uint32_t e8w[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const uint32_t x = tile0 + 128u * k + 4u * lane;
+        gv[k] = make_uint2(0u, 0u);
+        e8w[k] = 0u;
+        if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
+            gv[k] = ld_stream_u2(g + x);
+            e8w[k] = __ldcs(reinterpret_cast<const unsigned int *>(ef8 + x));
+        }
+    }
+    const f32x2 es2 = pack2(es, es), s2 = pack2(s, s);
+    const f32x2 unbias8 = pack2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+    f32x2 c[K][2], e[K][2];
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const uint32_t u = e8w[k] ^ 0x80808080u;  // stored error codes + 128
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const f32x2 f = pack2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440u + 2 * h)),
+                                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441u + 2 * h)));
+            e[k][h] = ops.mul(ops.add(f, unbias8), es2);  // stored error: code (exact) * scale
+            const uint32_t gw = h ? gv[k].y : gv[k].x;
+            const f32x2 gf = pack2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u));
+            c[k][h] = ops.add(gf, ops.mul(s2, e[k][h]));
+            float a, b;
+            unpack2(c[k][h], a, b);
+            m = max3(m, fabsf(a), fabsf(b));
+        }
+    }
+    m = group_max<kWarp>(m);
+    const BlockScale bs = block_scale<7>(m);
+    const f32x2 inv2 = pack2(bs.inv, bs.inv), sc2 = pack2(bs.scale, bs.scale);
+    const f32x2 shift4 = pack2(kRoundShift4, kRoundShift4);
+    const f32x2 unshift4 = pack2(-kRoundShift4, -kRoundShift4);
+    const f32x2 beta2 = pack2(beta, beta), omb2 = pack2(one_minus_beta, one_minus_beta);
+    f32x2 en[K][2];
+    float m8 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        uint32_t pr[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const f32x2 rq = ops.add(ops.mul(c[k][h], inv2), shift4);
+            float r0, r1;
+            unpack2(rq, r0, r1);
+            pr[h] = __float_as_uint(r0) + (__float_as_uint(r1) << 4);  // (q0 + 8) + 16 (q1 + 8)
+            const f32x2 d = ops.mul(ops.add(rq, unshift4), sc2);       // the code (exact) * scale
+            en[k][h] = ops.add(ops.mul(beta2, e[k][h]), ops.mul(omb2, ops.sub(c[k][h], d)));
+            float a, b;
+            unpack2(en[k][h], a, b);
+            m8 = max3(m8, fabsf(a), fabsf(b));
+        }
+        const uint32_t pos = out0 + 128u * k + 4u * lane;
+        if (WC_IN_BOUNDS(uint64_t(pos) + 4 <= geo.total))
+            __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2),
+                   (unsigned short)(__byte_perm(pr[0], pr[1], 0x0040u) ^ 0x8888u));
+    }
+    if (lane == 0 && WC_IN_BOUNDS(out0 / B < geo.total / B)) __stcs(scales + out0 / B, bs.scale);
+    // the new error of the block, quantized by the int8 absmax rule
+    m8 = group_max<kWarp>(m8);
+    const BlockScale bse = block_scale<127>(m8);
+    const f32x2 inv8 = pack2(bse.inv, bse.inv), shift8 = pack2(kRoundShift8, kRoundShift8);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        uint32_t rb[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float r0, r1;
+            unpack2(ops.add(ops.mul(en[k][h], inv8), shift8), r0, r1);
+            rb[2 * h] = __float_as_uint(r0);
+            rb[2 * h + 1] = __float_as_uint(r1);
+        }
+        const uint32_t x = tile0 + 128u * k + 4u * lane;
+        if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total))
+            __stcs(reinterpret_cast<unsigned int *>(ef8 + x), pack_int8_quad(rb[0], rb[1], rb[2], rb[3]));
+    }
+    if (lane == 0 && WC_IN_BOUNDS(eblk < geo.total / B)) __stcs(ef_scales + eblk, bse.scale);
+}
+
 template <int B, int EF>
 __device__ __forceinline__ void ef_quant_int4_warp(const uint16_t *__restrict__ g,
                                                    void *__restrict__ ef_v,
@@ -200,12 +315,27 @@ __device__ __forceinline__ void ef_quant_int4_warp(const uint16_t *__restrict__ 
 }
 
 template <int B, int EF>
+__device__ __forceinline__ void ef_quant_int4_body(const uint16_t *__restrict__ g,
+                                                   void *__restrict__ ef_v,
+                                                   float *__restrict__ ef_scales,
+                                                   uint8_t *__restrict__ codes,
+                                                   float *__restrict__ scales, QgzGeometry geo,
+                                                   float s, float beta, float one_minus_beta,
+                                                   const Exact2 &kc) {
+    if constexpr (EF == kEfInt8 && B >= 128)
+        ef_quant_int8ef_pairs<B>(g, static_cast<int8_t *>(ef_v), ef_scales, codes, scales, geo, s,
+                                 beta, one_minus_beta, kc);
+    else
+        ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
+}
+
+template <int B, int EF>
 __global__ void __launch_bounds__(256)
 ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                      float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
                      float *__restrict__ scales, QgzGeometry geo, float s, float beta,
-                     float one_minus_beta) {
-    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
+                     float one_minus_beta, Exact2 kc) {
+    ef_quant_int4_body<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta, kc);
 }
 
 // The bf16 and int8 error buffers move 2 and 1 bytes per element each way
@@ -218,8 +348,8 @@ __global__ void __launch_bounds__(256, 8)
 ef_quant_int4_resident8_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                                float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
                                float *__restrict__ scales, QgzGeometry geo, float s, float beta,
-                               float one_minus_beta) {
-    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
+                               float one_minus_beta, Exact2 kc) {
+    ef_quant_int4_body<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta, kc);
 }
 
 template <int B>
@@ -239,10 +369,11 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, f
         grid = dim3((tiles + threads / kWarp - 1) / (threads / kWarp));
     }
     const float omb = 1.0f - beta;
+    const Exact2 kc = exact2_constants();
     constexpr bool kResident8 = B == 128 || B == 256;
 #define WC_EFQ(KERNEL, MODE)                                                                   \
     KERNEL<B, MODE><<<grid, threads, 0, stream>>>(g, ef, ef_scales, codes, scales, geo, s, beta, \
-                                                   omb)
+                                                   omb, kc)
     if (ef == nullptr) WC_EFQ(ef_quant_int4_kernel, kEfNone);
     else if (ef_mode == kEfBf16 && kResident8) WC_EFQ(ef_quant_int4_resident8_kernel, kEfBf16);
     else if (ef_mode == kEfBf16) WC_EFQ(ef_quant_int4_kernel, kEfBf16);
