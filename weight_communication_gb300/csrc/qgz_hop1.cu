@@ -29,8 +29,11 @@
 // place of an unpack, an unbias, a multiply and an add.  The shuffles run on
 // the load/store pipe, so the last source takes the byte-permute path, in
 // packed form, on the ALU and FMA pipes.  The requantization is packed as
-// well (requantize_pairs).  Other shapes: a general kernel (lane groups of 8
-// consecutive outputs, sources fetched 8 at a time, scalar arithmetic).
+// well (requantize_pairs).  With its error buffer the hop is bound by HBM,
+// and the shuffles would compete with the error traffic for the load/store
+// pipe, so that form keeps the scalar byte-permute path.  Other shapes: a
+// general kernel (lane groups of 8 consecutive outputs, sources fetched 8 at
+// a time, scalar arithmetic).
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
@@ -144,28 +147,14 @@ __device__ __forceinline__ void requantize_lane(float p[E], uint32_t o, bool out
     if (out_ok && (lane & (LPB - 1)) == 0) __stcs(out_scales + o / B, bs.scale);
 }
 
-// requantize_lane on the E values of a lane held as E/2 packed pairs (p[j]:
-// values 2j, 2j+1), in packed exact arithmetic, with the codes packed through
-// the biased rounding of kRoundShift4: the same codes, scale and error
-// update bit for bit.  The whole warp holds one block (LPB = 32).
-template <int E, bool HAS_EF, int B>
-__device__ __forceinline__ void requantize_pairs(f32x2 p[E / 2], uint32_t o, bool out_ok, int lane,
-                                                 uint8_t *__restrict__ out_codes,
-                                                 float *__restrict__ out_scales,
-                                                 float *__restrict__ ef1, float s, float beta,
-                                                 float one_minus_beta, const Ops2 &ops) {
-    f32x2 e[HAS_EF ? E / 2 : 1];
-    if (HAS_EF) {
-        const f32x2 s2 = pack2(s, s);
-#pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-            const float4 v = out_ok ? ld_stream_f4(ef1 + o + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            e[2 * q] = pack2(v.x, v.y);
-            e[2 * q + 1] = pack2(v.z, v.w);
-        }
-#pragma unroll
-        for (int j = 0; j < E / 2; ++j) p[j] = ops.add(p[j], ops.mul(s2, e[HAS_EF ? j : 0]));
-    }
+// requantize_lane (without error feedback) on the E values of a lane held as
+// E/2 packed pairs (p[j]: values 2j, 2j+1), in packed exact arithmetic, with
+// the codes packed through the biased rounding of kRoundShift4: the same
+// codes and scale bit for bit.  The whole warp holds one block.
+template <int E, int B>
+__device__ __forceinline__ void requantize_pairs(const f32x2 p[E / 2], uint32_t o, bool out_ok,
+                                                 int lane, uint8_t *__restrict__ out_codes,
+                                                 float *__restrict__ out_scales, const Ops2 &ops) {
     float m = 0.0f;
 #pragma unroll
     for (int j = 0; j < E / 2; ++j) {
@@ -175,37 +164,21 @@ __device__ __forceinline__ void requantize_pairs(f32x2 p[E / 2], uint32_t o, boo
     }
     m = group_max<kWarp>(m);
     const BlockScale bs = block_scale<7>(m);
-    const f32x2 inv2 = pack2(bs.inv, bs.inv), sc2 = pack2(bs.scale, bs.scale);
-    const f32x2 shift = pack2(kRoundShift4, kRoundShift4), unshift = pack2(-kRoundShift4, -kRoundShift4);
-    const f32x2 beta2 = pack2(beta, beta), omb2 = pack2(one_minus_beta, one_minus_beta);
+    const f32x2 inv2 = pack2(bs.inv, bs.inv);
+    const f32x2 shift = pack2(kRoundShift4, kRoundShift4);
     uint32_t words[E / 8];
 #pragma unroll
     for (int wq = 0; wq < E / 8; ++wq) {
         uint32_t pairs[4];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const int j = 4 * wq + jj;
-            const f32x2 r = ops.add(ops.mul(p[j], inv2), shift);
             float r0, r1;
-            unpack2(r, r0, r1);
-            pairs[jj] = __float_as_uint(r0) + (__float_as_uint(r1) << 4);
-            if (HAS_EF) {
-                const f32x2 d = ops.mul(ops.add(r, unshift), sc2);  // the code (exact) * scale
-                p[j] = ops.add(ops.mul(beta2, e[HAS_EF ? j : 0]), ops.mul(omb2, ops.sub(p[j], d)));
-            }
+            unpack2(ops.add(ops.mul(p[4 * wq + jj], inv2), shift), r0, r1);
+            pairs[jj] = __float_as_uint(r0) + (__float_as_uint(r1) << 4);  // (q0 + 8) + 16 (q1 + 8)
         }
         words[wq] = pack_int4_pairs(pairs);
     }
     if (out_ok) store_words<E / 8>(out_codes + o / 2, words);
-    if (HAS_EF && out_ok) {
-#pragma unroll
-        for (int q = 0; q < E / 4; ++q) {
-            float a, b, c, d;
-            unpack2(p[2 * q], a, b);
-            unpack2(p[2 * q + 1], c, d);
-            __stcs(reinterpret_cast<float4 *>(ef1 + o + 4 * q), make_float4(a, b, c, d));
-        }
-    }
     if (out_ok && lane == 0) __stcs(out_scales + o / B, bs.scale);
 }
 
@@ -256,6 +229,29 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
             sc[t] = __ldg(sp + size_t(t) * sstride);
         }
     }
+    const bool out_ok = WC_IN_BOUNDS(uint64_t(o) + E <= uint64_t(geo.G) * geo.N);
+    if (HAS_EF) {
+        // With its error buffer the hop moves 8 more bytes per output and is
+        // bound by HBM; shuffles there compete with the error loads and
+        // stores for the load/store pipe and measured slower (0.77 -> 0.82 ms
+        // at B = 512, L = 8), so this form keeps the scalar byte-permute path.
+        float p[E];
+#pragma unroll
+        for (int t = 0; t < L; ++t) {
+#pragma unroll
+            for (int wq = 0; wq < W; ++wq) {
+                float f[8];
+                unpack_int4x8(w[t][wq], f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    p[8 * wq + j] = t == 0 ? dequant_first(f[j], sc[t])
+                                           : __fadd_rn(p[8 * wq + j], dequant(f[j], sc[t]));
+            }
+        }
+        requantize_lane<E, kWarp, HAS_EF, B>(p, o, out_ok, lane, out_codes, out_scales, ef1, s,
+                                             beta, one_minus_beta);
+        return;
+    }
     // The warp's E * 32 outputs are one block of every source, so each
     // source's products come from one warp-wide table.
     constexpr int NT = hop1_table_sources(L);
@@ -276,9 +272,7 @@ hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ s
             else accumulate_word<false, false, kWarp>(w[t][wq], table, s2, pw, kFull, ops);
         }
     }
-    const bool out_ok = WC_IN_BOUNDS(uint64_t(o) + E <= uint64_t(geo.G) * geo.N);
-    requantize_pairs<E, HAS_EF, B>(p, o, out_ok, lane, out_codes, out_scales, ef1, s, beta,
-                                   one_minus_beta, ops);
+    requantize_pairs<E, B>(p, o, out_ok, lane, out_codes, out_scales, ops);
 }
 
 // General shapes: warp tile T = max(B, 256) outputs, lane t holds outputs

@@ -43,46 +43,20 @@ enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2, kEfInt8 = 3 };
 // case of ef_quant_int4_warp, two elements per instruction, with the codes of
 // both quantizations packed through biased rounding (q + 8 and q + 128 in the
 // low byte).  Every code, scale and stored error is the one the scalar chain
-// gives, bit for bit.  Lane t holds elements 128k + 4t + j as pairs
-// (j = 0, 1) and (2, 3).
+// gives, bit for bit.  Lane t holds elements 128k + 4t + j of the block as
+// pairs (j = 0, 1) and (2, 3); the block's loads (gv: bf16 gradients, e8w:
+// stored error codes, es: stored error scale) are already in registers.
 template <int B>
-__device__ __forceinline__ void ef_quant_int8ef_pairs(const uint16_t *__restrict__ g,
-                                                      int8_t *__restrict__ ef8,
-                                                      float *__restrict__ ef_scales,
-                                                      uint8_t *__restrict__ codes,
-                                                      float *__restrict__ scales, QgzGeometry geo,
-                                                      float s, float beta, float one_minus_beta,
-                                                      const Exact2 &kc) {
-    static_assert(B >= 128 && B % 128 == 0, "one warp per block");
+__device__ __forceinline__ void int8ef_block(const uint2 (&gv)[B / 128],
+                                             const uint32_t (&e8w)[B / 128], float es,
+                                             int8_t *__restrict__ ef8,
+                                             float *__restrict__ ef_scales,
+                                             uint8_t *__restrict__ codes,
+                                             float *__restrict__ scales, const QgzGeometry &geo,
+                                             uint32_t tile0, uint32_t out0, int lane, float s,
+                                             float beta, float one_minus_beta, const Ops2 &ops) {
     constexpr int K = B / 128;
-    const int lane = threadIdx.x & (kWarp - 1);
-    const uint32_t off = (blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp) * B;
-    if (off >= geo.S) return;  // whole warp
-    const uint32_t slice = blockIdx.y, r = blockIdx.z;
-    uint32_t p = slice;
-    if (geo.G > 1) {
-        const uint32_t gq = slice / geo.L;
-        p = (slice - gq * geo.L) * geo.G + gq;
-    }
-    const uint32_t tile0 = r * geo.N + slice * geo.S + off;
-    const uint32_t out0 = r * geo.N + p * geo.S + off;
     const uint32_t eblk = tile0 / B;
-    const Ops2 ops(kc);
-
-    float es = 0.0f;
-    if (WC_IN_BOUNDS(eblk < geo.total / B)) es = __ldg(ef_scales + eblk);
-    uint2 gv[K];
-    uint32_t e8w[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-        const uint32_t x = tile0 + 128u * k + 4u * lane;
-        gv[k] = make_uint2(0u, 0u);
-        e8w[k] = 0u;
-        if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
-            gv[k] = ld_stream_u2(g + x);
-            e8w[k] = __ldcs(reinterpret_cast<const unsigned int *>(ef8 + x));
-        }
-    }
     const f32x2 es2 = pack2(es, es), s2 = pack2(s, s);
     const f32x2 unbias8 = pack2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
     f32x2 c[K][2], e[K][2];
@@ -151,6 +125,63 @@ __device__ __forceinline__ void ef_quant_int8ef_pairs(const uint16_t *__restrict
             __stcs(reinterpret_cast<unsigned int *>(ef8 + x), pack_int8_quad(rb[0], rb[1], rb[2], rb[3]));
     }
     if (lane == 0 && WC_IN_BOUNDS(eblk < geo.total / B)) __stcs(ef_scales + eblk, bse.scale);
+}
+
+// int8 error buffer, B >= 128: each warp takes NB consecutive blocks of a
+// slice and issues the loads of all of them before it computes the first.
+// A warp reads only 12 bytes per lane and block here, so with one block per
+// warp too few bytes are in flight to cover DRAM latency; at B = 256, two
+// blocks per warp under a budget of 4 CTAs per SM measured 0.388 -> 0.367 ms
+// (one block per warp with 8 CTAs per SM was the previous form).
+template <int B, int NB, int MINB>
+__global__ void __launch_bounds__(256, MINB)
+ef_quant_int8ef_kernel(const uint16_t *__restrict__ g, int8_t *__restrict__ ef8,
+                       float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
+                       float *__restrict__ scales, QgzGeometry geo, float s, float beta,
+                       float one_minus_beta, Exact2 kc) {
+    static_assert(B >= 128 && B % 128 == 0, "one warp per block");
+    constexpr int K = B / 128;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const uint32_t off0 = (blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp) * (B * NB);
+    if (off0 >= geo.S) return;  // whole warp
+    const uint32_t slice = blockIdx.y, r = blockIdx.z;
+    uint32_t p = slice;
+    if (geo.G > 1) {
+        const uint32_t gq = slice / geo.L;
+        p = (slice - gq * geo.L) * geo.G + gq;
+    }
+    const Ops2 ops(kc);
+    uint2 gv[NB][K];
+    uint32_t e8w[NB][K];
+    float es[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const uint32_t tile0 = r * geo.N + slice * geo.S + off0 + b * B;
+        es[b] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            gv[b][k] = make_uint2(0u, 0u);
+            e8w[b][k] = 0u;
+        }
+        if (off0 + b * B >= geo.S) continue;  // past the slice's last block (whole warp)
+        if (WC_IN_BOUNDS(tile0 / B < geo.total / B)) es[b] = __ldg(ef_scales + tile0 / B);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const uint32_t x = tile0 + 128u * k + 4u * lane;
+            if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
+                gv[b][k] = ld_stream_u2(g + x);
+                e8w[b][k] = __ldcs(reinterpret_cast<const unsigned int *>(ef8 + x));
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (off0 + b * B >= geo.S) break;
+        const uint32_t tile0 = r * geo.N + slice * geo.S + off0 + b * B;
+        const uint32_t out0 = r * geo.N + p * geo.S + off0 + b * B;
+        int8ef_block<B>(gv[b], e8w[b], es[b], ef8, ef_scales, codes, scales, geo, tile0, out0,
+                        lane, s, beta, one_minus_beta, ops);
+    }
 }
 
 template <int B, int EF>
@@ -315,27 +346,12 @@ __device__ __forceinline__ void ef_quant_int4_warp(const uint16_t *__restrict__ 
 }
 
 template <int B, int EF>
-__device__ __forceinline__ void ef_quant_int4_body(const uint16_t *__restrict__ g,
-                                                   void *__restrict__ ef_v,
-                                                   float *__restrict__ ef_scales,
-                                                   uint8_t *__restrict__ codes,
-                                                   float *__restrict__ scales, QgzGeometry geo,
-                                                   float s, float beta, float one_minus_beta,
-                                                   const Exact2 &kc) {
-    if constexpr (EF == kEfInt8 && B >= 128)
-        ef_quant_int8ef_pairs<B>(g, static_cast<int8_t *>(ef_v), ef_scales, codes, scales, geo, s,
-                                 beta, one_minus_beta, kc);
-    else
-        ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
-}
-
-template <int B, int EF>
 __global__ void __launch_bounds__(256)
 ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                      float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
                      float *__restrict__ scales, QgzGeometry geo, float s, float beta,
-                     float one_minus_beta, Exact2 kc) {
-    ef_quant_int4_body<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta, kc);
+                     float one_minus_beta) {
+    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
 }
 
 // The bf16 and int8 error buffers move 2 and 1 bytes per element each way
@@ -348,8 +364,8 @@ __global__ void __launch_bounds__(256, 8)
 ef_quant_int4_resident8_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                                float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
                                float *__restrict__ scales, QgzGeometry geo, float s, float beta,
-                               float one_minus_beta, Exact2 kc) {
-    ef_quant_int4_body<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta, kc);
+                               float one_minus_beta) {
+    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
 }
 
 template <int B>
@@ -369,15 +385,23 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, f
         grid = dim3((tiles + threads / kWarp - 1) / (threads / kWarp));
     }
     const float omb = 1.0f - beta;
-    const Exact2 kc = exact2_constants();
     constexpr bool kResident8 = B == 128 || B == 256;
+    if (ef != nullptr && ef_mode == kEfInt8 && B >= 128) {
+        // two blocks per warp at B = 128 and 256 (see ef_quant_int8ef_kernel)
+        constexpr int NB = kResident8 ? 2 : 1;
+        const uint32_t warps = (geo.S / B + NB - 1) / NB;
+        const dim3 g8((warps + threads / kWarp - 1) / (threads / kWarp), geo.R, geo.R);
+        ef_quant_int8ef_kernel<(B >= 128 ? B : 128), NB, (kResident8 ? 4 : 1)>
+            <<<g8, threads, 0, stream>>>(g, static_cast<int8_t *>(ef), ef_scales, codes, scales,
+                                         geo, s, beta, omb, exact2_constants());
+        return cudaPeekAtLastError();
+    }
 #define WC_EFQ(KERNEL, MODE)                                                                   \
     KERNEL<B, MODE><<<grid, threads, 0, stream>>>(g, ef, ef_scales, codes, scales, geo, s, beta, \
-                                                   omb, kc)
+                                                   omb)
     if (ef == nullptr) WC_EFQ(ef_quant_int4_kernel, kEfNone);
     else if (ef_mode == kEfBf16 && kResident8) WC_EFQ(ef_quant_int4_resident8_kernel, kEfBf16);
     else if (ef_mode == kEfBf16) WC_EFQ(ef_quant_int4_kernel, kEfBf16);
-    else if (ef_mode == kEfInt8 && kResident8) WC_EFQ(ef_quant_int4_resident8_kernel, kEfInt8);
     else if (ef_mode == kEfInt8) WC_EFQ(ef_quant_int4_kernel, kEfInt8);
     else WC_EFQ(ef_quant_int4_kernel, kEfF32);
 #undef WC_EFQ

@@ -15,16 +15,19 @@
 //
 // The per-code work -- unpack, multiply by the scale, add in source order --
 // is all the kernel does besides moving bytes, so it runs issue-bound unless
-// the instruction count per code stays near its floor of one byte permute
-// and three exact fp32 operations (two for the first source, whose add to
-// the +0 start folds into one fma).  Hence: the source count is a template
+// the instructions per code stay few.  Hence: the source count is a template
 // parameter (no loop bounds, no guards, every load hoisted ahead of the
 // adds), each thread makes 16 consecutive outputs from one 8-byte code word
 // per source (so the per-source address and scale work is amortized over 16
 // codes), the destination comes from the grid's y index (no division), and
 // codes are unpacked with byte permutes and exact subtractions
-// (wc_device.cuh), never on the conversion pipe.  Source counts above
-// kMaxFixedSources take a loop over batches of eight.
+// (wc_device.cuh), never on the conversion pipe.  For 3 to 8 sources and
+// blocks of 256 or more the sums run two outputs per packed instruction
+// (byte permute, then an exact packed unbias, multiply and add per pair of
+// codes), and the first source's products come from a half-warp product
+// table instead (each half-warp's 256 outputs lie in one block of every
+// source); that kernel takes a register budget for 5 CTAs per SM.  Source
+// counts above kMaxFixedSources take a loop over batches of eight.
 #include "wc_device.cuh"
 #include "wc_internal.h"
 
@@ -92,6 +95,61 @@ __device__ __forceinline__ bool source_in_bounds(const QgzGeometry &geo, uint32_
 
 __device__ __forceinline__ bool output_in_bounds(const QgzGeometry &geo, uint32_t k, uint32_t i) {
     return uint64_t(k) * geo.S + i + kOutPerThread <= geo.N;
+}
+
+// The same sums two outputs at a time (acc[j]: outputs 2j, 2j+1), for 3..8
+// sources and B >= 256.  S is then a multiple of 256, so every half-warp is
+// wholly inside the shard or wholly past it, and the 256 outputs of a
+// half-warp lie in one block of every source: the first source's products
+// come from the half-warp's product table (one 16-wide shuffle per code),
+// the others from the packed byte-permute path (accumulate_word).  Measured
+// at 8 sources and B = 256: 0.0758 -> 0.0695 ms.  The budget of 5 CTAs per
+// SM matters: unbounded, the compiler's allocation took it to 0.164 ms.
+template <int NSRC, bool OUT_BF16, bool SCALED>
+__global__ void __launch_bounds__(256, 5)
+dequant_reduce_pairs_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
+                            QgzGeometry geo, uint32_t log2_b, float out_scale,
+                            void *__restrict__ out, Exact2 kc) {
+    const uint32_t k = blockIdx.y;  // destination
+    const uint32_t v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (uint64_t(v) * kOutPerThread >= geo.S) return;  // whole half-warps
+    const uint32_t i = v * kOutPerThread;
+    const uint32_t base = source_base(geo, k, i);
+    const uint8_t *cp = codes + base / 2;
+    const float *sp = scales + (base >> log2_b);
+    const uint32_t cstride = geo.N / 2;
+    const uint32_t sstride = geo.N >> log2_b;
+    uint2 w[NSRC];
+    float sc[NSRC];
+#pragma unroll
+    for (int t = 0; t < NSRC; ++t) {
+        w[t] = make_uint2(0u, 0u);
+        sc[t] = 0.0f;
+        if (WC_IN_BOUNDS(source_in_bounds(geo, base, t))) {
+            w[t] = __ldcs(reinterpret_cast<const uint2 *>(cp + size_t(t) * cstride));
+            sc[t] = __ldg(sp + size_t(t) * sstride);
+        }
+    }
+    const Ops2 ops(kc);
+    const int lane = threadIdx.x & (kWarp - 1);
+    const unsigned hmask = 0xFFFFu << (lane & 16);
+    f32x2 a2[8];
+    {
+        const float table = product_table<true>(sc[0], lane);
+        accumulate_word<true, true, 16>(w[0].x, table, pack2(0.0f, 0.0f), a2, hmask, ops);
+        accumulate_word<true, true, 16>(w[0].y, table, pack2(0.0f, 0.0f), a2 + 4, hmask, ops);
+    }
+#pragma unroll
+    for (int t = 1; t < NSRC; ++t) {
+        const f32x2 s2 = pack2(sc[t], sc[t]);
+        accumulate_word<false, false, 16>(w[t].x, 0.0f, s2, a2, hmask, ops);
+        accumulate_word<false, false, 16>(w[t].y, 0.0f, s2, a2 + 4, hmask, ops);
+    }
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) unpack2(a2[j], acc[2 * j], acc[2 * j + 1]);
+    if (WC_IN_BOUNDS(output_in_bounds(geo, k, i)))
+        store16<OUT_BF16, SCALED>(out, k * geo.S + i, acc, out_scale);
 }
 
 template <int NSRC, bool OUT_BF16, bool SCALED>
@@ -174,8 +232,13 @@ template <int NSRC, bool OUT_BF16, bool SCALED>
 static void launch_fixed(const uint8_t *codes, const float *scales, const QgzGeometry &geo,
                          uint32_t log2_b, float out_scale, void *out, dim3 grid,
                          cudaStream_t stream) {
-    dequant_reduce_fixed_kernel<NSRC, OUT_BF16, SCALED><<<grid, 256, 0, stream>>>(
-        codes, scales, geo, log2_b, out_scale, out);
+    if (NSRC >= 3 && NSRC <= 8 && log2_b >= 8)  // B >= 256
+        dequant_reduce_pairs_kernel<(NSRC >= 3 && NSRC <= 8 ? NSRC : 3), OUT_BF16, SCALED>
+            <<<grid, 256, 0, stream>>>(codes, scales, geo, log2_b, out_scale, out,
+                                       exact2_constants());
+    else
+        dequant_reduce_fixed_kernel<NSRC, OUT_BF16, SCALED><<<grid, 256, 0, stream>>>(
+            codes, scales, geo, log2_b, out_scale, out);
 }
 
 template <bool OUT_BF16, bool SCALED>
