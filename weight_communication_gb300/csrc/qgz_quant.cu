@@ -130,9 +130,10 @@ __device__ __forceinline__ void int8ef_block(const uint2 (&gv)[B / 128],
 // int8 error buffer, B >= 128: each warp takes NB consecutive blocks of a
 // slice and issues the loads of all of them before it computes the first.
 // A warp reads only 12 bytes per lane and block here, so with one block per
-// warp too few bytes are in flight to cover DRAM latency; at B = 256, two
-// blocks per warp under a budget of 4 CTAs per SM measured 0.388 -> 0.367 ms
-// (one block per warp with 8 CTAs per SM was the previous form).
+// warp too few bytes are in flight to cover DRAM latency.  At B = 256, timed
+// back to back: one block per warp under a budget of 8 CTAs per SM 0.388 ms,
+// two blocks with 4 CTAs 0.367-0.380 ms, three blocks with 3 CTAs 0.353 ms,
+// four blocks with 2 or 3 CTAs 0.365 ms.
 template <int B, int NB, int MINB>
 __global__ void __launch_bounds__(256, MINB)
 ef_quant_int8ef_kernel(const uint16_t *__restrict__ g, int8_t *__restrict__ ef8,
@@ -387,11 +388,11 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, f
     const float omb = 1.0f - beta;
     constexpr bool kResident8 = B == 128 || B == 256;
     if (ef != nullptr && ef_mode == kEfInt8 && B >= 128) {
-        // two blocks per warp at B = 128 and 256 (see ef_quant_int8ef_kernel)
-        constexpr int NB = kResident8 ? 2 : 1;
+        // three blocks per warp at B = 128 and 256 (see ef_quant_int8ef_kernel)
+        constexpr int NB = kResident8 ? 3 : 1;
         const uint32_t warps = (geo.S / B + NB - 1) / NB;
         const dim3 g8((warps + threads / kWarp - 1) / (threads / kWarp), geo.R, geo.R);
-        ef_quant_int8ef_kernel<(B >= 128 ? B : 128), NB, (kResident8 ? 4 : 1)>
+        ef_quant_int8ef_kernel<(B >= 128 ? B : 128), NB, (kResident8 ? 3 : 1)>
             <<<g8, threads, 0, stream>>>(g, static_cast<int8_t *>(ef), ef_scales, codes, scales,
                                          geo, s, beta, omb, exact2_constants());
         return cudaPeekAtLastError();
