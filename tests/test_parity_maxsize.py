@@ -173,3 +173,110 @@ def test_small_blocks_at_the_largest_size(dev):
                           f"qwZ dequantized block {b}")
     del w, qc, qs, back
     torch.cuda.empty_cache()
+
+
+def _random_codes(n_bytes: int, seed: int, dev) -> torch.Tensor:
+    """n_bytes random code bytes on the device (every nibble, -8 included)."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    return torch.randint(0, 256, (n_bytes,), dtype=torch.uint8, device=dev, generator=gen)
+
+
+def _random_scales(n: int, seed: int, dev) -> torch.Tensor:
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    return (torch.randn(n, device=dev, generator=gen) * 1e-3).to(torch.float32)
+
+
+def test_packed_kernels_at_the_largest_size(dev):
+    """The packed and product-table kernels where 32-bit indexing ends: the
+    packed flat reduce (4 sources, B = 256), the first hop's table path
+    (16 ranks in 2 groups, B = 512) and the int8 error buffer's kernel
+    (three blocks per warp, B = 256), each with R*N just under 2^32.
+    Sampled blocks at the start and the end of shards and units are
+    recomputed by the oracle as small problems of their own."""
+    # packed flat reduce, R = 4, R*N = 2^32 - 4096
+    R, B = 4, 256
+    N = (1 << 30) - 1024
+    S = N // R
+    codes = _random_codes(R * N // 2, 7700, dev)
+    scales = _random_scales(R * N // B, 7701, dev)
+    out = torch.empty(N, dtype=torch.float32, device=dev)
+    binding.dequant_reduce(codes, scales, out, N, R, 1, B)
+    torch.cuda.synchronize()
+    for k in (0, R - 1):
+        for j in (0, S // B - 1):
+            mc = np.zeros(R * R * B // 2, np.uint8)
+            ms = np.ones(R * R, np.float32)
+            for r in range(R):
+                src = r * N + k * S + j * B
+                mc[r * R * B // 2:(r * R * B + B) // 2] = to_host(codes[src // 2:(src + B) // 2])
+                ms[r * R] = to_host(scales[src // B:src // B + 1])[0]
+            want = ORC.dequant_reduce(mc, ms, R * B, R, 1, B)[:B]
+            o0 = k * S + j * B
+            assert_bits_equal(to_host(out[o0:o0 + B]), want, f"packed reduce shard {k} block {j}")
+    del codes, scales, out
+    torch.cuda.empty_cache()
+
+    # first hop through product tables: R = 16, G = 2, L = 8, R*N = 2^32 - 131072
+    R, G, B = 16, 2, 512
+    L = R // G
+    N = (1 << 28) - 8192
+    S = N // R
+    codes = _random_codes(R * N // 2, 7702, dev)
+    scales = _random_scales(R * N // B, 7703, dev)
+    c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    binding.dequant_reduce_requant(codes, scales, c1, s1, N, R, G, B)
+    torch.cuda.synchronize()
+    for u in (0, R - 1):
+        grp, l = divmod(u, L)
+        for gq in (0, G - 1):
+            for j in (0, S // B - 1):
+                # one group of L ranks whose chunk 0 is the unit's source block
+                mc = np.zeros(L * L * B // 2, np.uint8)
+                ms = np.ones(L * L, np.float32)
+                for lq in range(L):
+                    src = (grp * L + lq) * N + (l * G + gq) * S + j * B
+                    mc[lq * L * B // 2:(lq * L * B + B) // 2] = to_host(codes[src // 2:(src + B) // 2])
+                    ms[lq * L] = to_host(scales[src // B:src // B + 1])[0]
+                oc, os_ = ORC.dequant_reduce_requant(mc, ms, L * B, L, 1, B)
+                dst = (u * G + gq) * S + j * B
+                assert_bits_equal(to_host(c1[dst // 2:(dst + B) // 2]), oc[:B // 2],
+                                  f"table hop 1 u={u} gq={gq} j={j}")
+                assert_bits_equal(to_host(s1[dst // B:dst // B + 1]), os_[:1],
+                                  f"table hop 1 scale u={u} gq={gq} j={j}")
+    del codes, scales, c1, s1
+    torch.cuda.empty_cache()
+
+    # int8 error buffer, R = 4, R*N = 2^32 - 4096, stored errors random
+    R, B, s, beta = 4, 256, 1.0, 0.5
+    N = (1 << 30) - 1024
+    S = N // R
+    g = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+    for r in range(R):
+        wl.draw_bf16(N, 1e-3, 7800 + r, dev, out=g[r])
+    gf = g.view(-1)
+    e8 = _random_codes(R * N, 7810, dev).view(torch.int8)
+    es = (_random_scales(R * N // B, 7811, dev).abs() * 1e-2).contiguous()
+    e8_0 = {}
+    es_0 = {}
+    picks = [(r, b) for r in (0, R - 1) for b in (0, S // B - 1, N // B - 1)]
+    for r, b in picks:
+        x0 = r * N + b * B
+        e8_0[(r, b)] = to_host(e8[x0:x0 + B]).copy()
+        es_0[(r, b)] = to_host(es[x0 // B:x0 // B + 1]).copy()
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    binding.ef_quant_int4_int8ef(gf, e8, es, codes, scales, N, R, 1, B, s, beta)
+    torch.cuda.synchronize()
+    for r, b in picks:
+        x0 = r * N + b * B
+        e8c, esc = e8_0[(r, b)].copy(), es_0[(r, b)].copy()
+        cc, cs = ORC.ef_quant_int4_int8ef(to_host(gf[x0:x0 + B]).copy(), e8c, esc, B, 1, 1, B, s, beta)
+        assert_bits_equal(to_host(codes[x0 // 2:(x0 + B) // 2]), cc, f"int8-EF codes r={r} b={b}")
+        assert_bits_equal(to_host(scales[x0 // B:x0 // B + 1]), cs, f"int8-EF scale r={r} b={b}")
+        assert_bits_equal(to_host(e8[x0:x0 + B]), e8c, f"int8 error r={r} b={b}")
+        assert_bits_equal(to_host(es[x0 // B:x0 // B + 1]), esc, f"int8 error scale r={r} b={b}")
+    del g, e8, es, codes, scales
+    torch.cuda.empty_cache()
