@@ -187,14 +187,19 @@ __device__ __forceinline__ void requantize_pairs(const f32x2 p[E / 2], uint32_t 
 // byte-permute path on the ALU and FMA pipes instead).
 __host__ __device__ constexpr int hop1_table_sources(int L) { return L - (L + 7) / 8; }
 
-// Launch bounds: a budget for 5 CTAs per SM (at most 51 registers) at B <= 512
+// Launch bounds: a budget for 1280 threads per SM (at most 51 registers) at B <= 512
 // measured faster than the compiler's unbounded choice -- at B = 512, L = 8,
 // 0.594 -> 0.574 ms without error feedback (48 registers instead of 40) and
 // 0.815 -> 0.773 ms with it (48 with 4 bytes of spills, instead of 55 and 4
-// CTAs).  A budget for 6 CTAs was slower with error feedback.  B = 1024 needs
-// about 110 registers and takes no budget.
+// CTAs of 256 threads).  A budget for 6 such CTAs was slower with error
+// feedback.  B = 1024 needs about 110 registers and takes no budget.
+// CTAs of 128 threads: with the same register budget (10 CTAs of 128
+// threads per SM) they measured 0.447 -> 0.441 ms against 256-thread CTAs,
+// bit-identical (more CTAs per SM start and stall at different times).
+constexpr int kHop1Threads = 128;
+
 template <int B, int L, bool HAS_EF>
-__global__ void __launch_bounds__(256, B <= 512 ? 5 : 1)
+__global__ void __launch_bounds__(kHop1Threads, B <= 512 ? 10 : 1)
 hop1_fixed_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                   uint8_t *__restrict__ out_codes, float *__restrict__ out_scales,
                   QgzGeometry geo, float *__restrict__ ef1, float s, float beta,
@@ -388,12 +393,13 @@ static bool launch_fixed_b(const uint8_t *codes, const float *scales, uint8_t *o
                            float *out_scales, const QgzGeometry &geo, float *ef1, float s,
                            float beta, cudaStream_t stream) {
     const uint32_t warps = geo.S / B;  // per sub-slice
-    const dim3 grid((warps + 7) / 8, geo.G, geo.R);
+    constexpr uint32_t kWarpsPerCta = kHop1Threads / kWarp;
+    const dim3 grid((warps + kWarpsPerCta - 1) / kWarpsPerCta, geo.G, geo.R);
     const float omb = 1.0f - beta;
     const Exact2 kc = exact2_constants();
 #define WC_HOP1(LL)                                                                           \
     case LL:                                                                                  \
-        hop1_fixed_kernel<B, LL, HAS_EF><<<grid, 256, 0, stream>>>(codes, scales, out_codes,  \
+        hop1_fixed_kernel<B, LL, HAS_EF><<<grid, kHop1Threads, 0, stream>>>(codes, scales, out_codes,  \
                                                                    out_scales, geo, ef1, s,   \
                                                                    beta, omb, kc);            \
         return true;
@@ -401,7 +407,7 @@ static bool launch_fixed_b(const uint8_t *codes, const float *scales, uint8_t *o
         WC_HOP1(1) WC_HOP1(2) WC_HOP1(4) WC_HOP1(8)
         case 16:
             if (B > 512) return false;  // 16 sources x 4 words would not fit in registers
-            hop1_fixed_kernel<B, (B > 512 ? 8 : 16), HAS_EF><<<grid, 256, 0, stream>>>(
+            hop1_fixed_kernel<B, (B > 512 ? 8 : 16), HAS_EF><<<grid, kHop1Threads, 0, stream>>>(
                 codes, scales, out_codes, out_scales, geo, ef1, s, beta, omb, kc);
             return true;
         default:

@@ -26,7 +26,8 @@
 // (byte permute, then an exact packed unbias, multiply and add per pair of
 // codes), and the first source's products come from a half-warp product
 // table instead (each half-warp's 256 outputs lie in one block of every
-// source); that kernel takes a register budget for 5 CTAs per SM.  Source
+// source); that kernel takes CTAs of 128 threads and a register budget for
+// 10 of them per SM.  Source
 // counts above kMaxFixedSources take a loop over batches of eight.
 #include "wc_device.cuh"
 #include "wc_internal.h"
@@ -103,10 +104,14 @@ __device__ __forceinline__ bool output_in_bounds(const QgzGeometry &geo, uint32_
 // half-warp lie in one block of every source: the first source's products
 // come from the half-warp's product table (one 16-wide shuffle per code),
 // the others from the packed byte-permute path (accumulate_word).  Measured
-// at 8 sources and B = 256: 0.0758 -> 0.0695 ms.  The budget of 5 CTAs per
-// SM matters: unbounded, the compiler's allocation took it to 0.164 ms.
+// at 8 sources and B = 256: 0.0758 -> 0.0695 ms.  The register budget (1280
+// threads per SM) matters: unbounded, the compiler's allocation took it to
+// 0.164 ms.  CTAs of 128 threads (10 per SM) in place of 256 (5 per SM):
+// 0.0689 -> 0.0670 ms, bit-identical.
+constexpr uint32_t kPairsThreads = 128;
+
 template <int NSRC, bool OUT_BF16, bool SCALED>
-__global__ void __launch_bounds__(256, 5)
+__global__ void __launch_bounds__(kPairsThreads, 10)
 dequant_reduce_pairs_kernel(const uint8_t *__restrict__ codes, const float *__restrict__ scales,
                             QgzGeometry geo, uint32_t log2_b, float out_scale,
                             void *__restrict__ out, Exact2 kc) {
@@ -232,13 +237,15 @@ template <int NSRC, bool OUT_BF16, bool SCALED>
 static void launch_fixed(const uint8_t *codes, const float *scales, const QgzGeometry &geo,
                          uint32_t log2_b, float out_scale, void *out, dim3 grid,
                          cudaStream_t stream) {
-    if (NSRC >= 3 && NSRC <= 8 && log2_b >= 8)  // B >= 256
+    if (NSRC >= 3 && NSRC <= 8 && log2_b >= 8) {  // B >= 256
+        const dim3 pgrid((geo.S / kOutPerThread + kPairsThreads - 1) / kPairsThreads, grid.y);
         dequant_reduce_pairs_kernel<(NSRC >= 3 && NSRC <= 8 ? NSRC : 3), OUT_BF16, SCALED>
-            <<<grid, 256, 0, stream>>>(codes, scales, geo, log2_b, out_scale, out,
-                                       exact2_constants());
-    else
+            <<<pgrid, kPairsThreads, 0, stream>>>(codes, scales, geo, log2_b, out_scale, out,
+                                                  exact2_constants());
+    } else {
         dequant_reduce_fixed_kernel<NSRC, OUT_BF16, SCALED><<<grid, 256, 0, stream>>>(
             codes, scales, geo, log2_b, out_scale, out);
+    }
 }
 
 template <bool OUT_BF16, bool SCALED>
