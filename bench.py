@@ -9,11 +9,12 @@ per second (R*N per step) through both kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload qgz_single_hop|qgz_fused|qgz_bf16ef|qgz_int8ef|qgz_hier_ef|
-                                qgz_tiny|qgz_hierarchical|qwz|sr|all]
+                                qgz_hier_fused|qgz_tiny|qgz_hierarchical|qwz|sr|all]
 
 The other workloads: the same step as one fused kernel (qgz_fused), with a
 bf16 or an int8 error buffer (qgz_bf16ef, qgz_int8ef), the 16-rank two-hop reduce without and with
-first-hop error feedback (qgz_hierarchical, qgz_hier_ef), the L2-resident
+first-hop error feedback (qgz_hierarchical, qgz_hier_ef), the same with its
+first stage as one kernel (qgz_hier_fused), the L2-resident
 4-rank step (qgz_tiny), the qwZ int8 round trip and one-pass replica (qwz),
 and the bf16 stochastic-rounding accumulate (sr).
 
@@ -534,6 +535,72 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
             "gpu_launches": args.steps, "clocks": clocks}, None
 
 
+def run_qgz_hier_fused(w: wl.QgzWorkload, args, dev, dist, ws):
+    """The hierarchical step with its first stage as one kernel (every rank's
+    EF-quant fused with the first hop, writing the error buffers, the send
+    buffers and the first hop's output), then the second hop."""
+    from weight_communication_gb300 import binding
+    assert w.G > 1
+    ef = torch.zeros(w.R * w.N, dtype=torch.float32, device=dev)
+    codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+    c1 = torch.empty(w.G * w.N // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(w.G * w.N // w.B, dtype=torch.float32, device=dev)
+    out = torch.empty(w.N, dtype=torch.bfloat16 if w.out_bf16 else torch.float32, device=dev)
+    nbatch = max(1, min(args.batches, (8 << 30) // (w.R * w.N * 2)))
+    batches = [wl.qgz_gradients(w, t, device=dev) for t in range(nbatch)]
+    stream = torch.cuda.Stream(dev)
+    names = ["qgz_first_hop_fused", "dequant_reduce"]
+    with torch.cuda.stream(stream):
+        def step(i, timer=None, ti=None):
+            if timer is not None:
+                timer.mark(ti, 0)
+            binding.qgz_first_hop_fused(batches[i % nbatch].view(-1), ef, codes, scales, c1, s1,
+                                        w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, stream)
+            if timer is not None:
+                timer.mark(ti, 1)
+            binding.dequant_reduce(c1, s1, out, w.N, w.R, w.G, w.B, 1.0, stream)
+            if timer is not None:
+                timer.mark(ti, 2)
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        timer = Timer(names, args.steps)
+        sampler = clocks_begin(args, dev)
+        barrier(dist)
+        t0 = time.time()
+        for i in range(args.steps):
+            step(args.warmup + i, timer, i)
+        torch.cuda.synchronize(dev)
+        t1 = time.time()
+        barrier(dist)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
+    per = timer.per_kernel_ms()
+    pct = timer.per_kernel_percentiles()
+    peak, kind = measured_peaks()
+    kb = {"qgz_first_hop_fused": int(w.R * w.N * (2 + 8 + 0.5) + w.R * w.N // w.B * 4
+                                     + w.G * w.N * (0.5 + 4 / w.B)),
+          "dequant_reduce": int(w.N * (w.G * (0.5 + 4 / w.B) + (2 if w.out_bf16 else 4)))}
+    kernels = {n: {"ms": round(per[n], 5), "ms_percentiles": pct[n], "algorithmic_bytes": kb[n],
+                   "GB/s": round(kb[n] / (per[n] / 1e3) / 1e9, 1),
+                   "frac": round(kb[n] / (per[n] / 1e3) / 1e9 / peak, 4)} for n in names}
+    return {"metric": METRIC + " [hierarchical, fused first stage]",
+            "value": job_throughput(w.R * w.N, ws, ms), "unit": "elements/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded normal gradients with sparse outliers)",
+            "config": {"workload": w.name + " fused first stage", "R": w.R, "N": w.N, "G": w.G,
+                       "B": w.B, "err_scale": w.err_scale, "err_beta": w.err_beta,
+                       "l2": f"inputs exceed L2 ({w.R * w.N * 10 / 1e9:.1f} GB per step)"},
+            "roofline": {"bound": "hbm", "kernel": "qgz_first_hop_fused",
+                         "achieved": kernels["qgz_first_hop_fused"]["GB/s"], "peak": peak,
+                         "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
+                         "frac": kernels["qgz_first_hop_fused"]["frac"], "traffic": None,
+                         "algorithmic_bytes": kb["qgz_first_hop_fused"]},
+            "kernels": kernels, "gpu_launches": 2 * args.steps, "clocks": clocks}, None
+
+
 def parse_cpulist(text: str) -> list[int]:
     """'0-3,8,10-11' -> [0, 1, 2, 3, 8, 10, 11]."""
     cpus = []
@@ -759,6 +826,85 @@ def qgz_parity_on_sample(w: wl.QgzWorkload, fraction: int, steps: int, dev) -> d
     return gpu_parity_on_sample(sw, g, steps, out, ef, dev)
 
 
+def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, steps: int,
+                             dev) -> dict:
+    """`steps` chained steps of a 1/fraction sample of w through one of the
+    step's other forms, oracle against the CUDA path: every shard and every
+    element of every error buffer the form keeps.
+      hier_ef    -- the two-hop step with the first hop's own error buffer
+      bf16ef     -- the step with a bf16 error buffer
+      int8ef     -- the step with an int8 error buffer and a scale per block
+      fused      -- the flat step as one kernel (wc_qgz_step_fused)
+      hier_fused -- the two-hop step with its first stage as one kernel
+                    (wc_qgz_first_hop_fused), then the second hop"""
+    import oracle
+    from weight_communication_gb300 import binding
+    from weight_communication_gb300.qgz import QgzReducer
+    orc = oracle.get()
+    sw = qgz_sample(w, fraction)
+    N, R, G, B, s, beta = sw.N, sw.R, sw.G, sw.B, sw.err_scale, sw.err_beta
+    g = wl.as_u16(wl.qgz_gradients(sw, 0)).ravel().copy()
+    bufs = {}                                     # oracle error buffers by name
+    if variant == "bf16ef":
+        bufs["ef"] = np.zeros(R * N, np.uint16)
+    elif variant == "int8ef":
+        bufs["ef"] = np.zeros(R * N, np.int8)
+        bufs["ef_scales"] = np.zeros(R * N // B, np.float32)
+    else:
+        bufs["ef"] = np.zeros(R * N, np.float32)
+    if variant == "hier_ef":
+        bufs["ef1"] = np.zeros(G * N, np.float32)
+    for _ in range(steps):
+        if variant == "bf16ef":
+            codes, scales = orc.ef_quant_int4_bf16ef(g, bufs["ef"], N, R, G, B, s, beta)
+        elif variant == "int8ef":
+            codes, scales = orc.ef_quant_int4_int8ef(g, bufs["ef"], bufs["ef_scales"], N, R, G,
+                                                     B, s, beta)
+        else:
+            codes, scales = orc.ef_quant_int4(g, bufs["ef"], N, R, G, B, s, beta)
+        if G > 1:
+            codes, scales = orc.dequant_reduce_requant_ef(codes, scales, N, R, G, B,
+                                                          bufs.get("ef1"), s, beta)
+        want = orc.dequant_reduce(codes, scales, N, R, G, B, 1.0, sw.out_bf16)
+    out_dtype = torch.bfloat16 if sw.out_bf16 else torch.float32
+    gd = wl.from_u16(g, dev)
+    got = {}
+    if variant in ("fused", "hier_fused"):
+        ef = torch.zeros(R * N, dtype=torch.float32, device=dev)
+        out = torch.empty(N, dtype=out_dtype, device=dev)
+        c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+        s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+        for _ in range(steps):
+            if variant == "fused":
+                binding.qgz_step_fused(gd, ef, None, None, out, N, R, B, s, beta)
+            else:
+                binding.qgz_first_hop_fused(gd, ef, None, None, c1, s1, N, R, G, B, s, beta)
+                binding.dequant_reduce(c1, s1, out, N, R, G, B)
+        got["ef"] = ef
+    else:
+        ef_dtype = {"bf16ef": torch.bfloat16, "int8ef": torch.int8}.get(variant, torch.float32)
+        red = QgzReducer(N, R, G, B, s, beta, out_dtype=out_dtype, device=dev,
+                         ef_dtype=ef_dtype, hop1_ef=variant == "hier_ef")
+        gv = gd.view(R, N)
+        for _ in range(steps):
+            red.step(gv)
+        out = red.out
+        got["ef"] = red.ef
+        if variant == "int8ef":
+            got["ef_scales"] = red.ef_scales
+        if variant == "hier_ef":
+            got["ef1"] = red.ef1
+    torch.cuda.synchronize(dev)
+    same = {"shards": np.array_equal(np.ascontiguousarray(out.cpu().view(torch.uint8).numpy()),
+                                     want.view(np.uint8))}
+    for name, t in got.items():
+        same[name] = np.array_equal(t.cpu().view(torch.uint8).numpy(), bufs[name].view(np.uint8))
+    return {"verdict": "bit-exact" if all(same.values()) else "MISMATCH",
+            **{k: bool(v) for k, v in same.items()},
+            "compared": f"every shard and error-buffer element after {steps} steps of a 1/{fraction} "
+                        f"sample (R={R}, N={N}), against the oracle"}
+
+
 def qwz_parity(w: wl.QwzWorkload, tensors, dev) -> dict:
     """Sampled block ranges (the first and the last 2^20 weights) of the
     full-size qwZ run against the oracle: the one-pass replica kernel's codes,
@@ -814,7 +960,7 @@ def other_workloads(args, dev, dist, ws, rank) -> dict:
     plus the single-hop step's low-precision error buffers and fused form:
     per kernel the mean and median event time, algorithmic bytes and fraction
     of the HBM peak, over at most 20 timed steps each.  With the CPU legs on
-    (rank 0 of a single process), the first three also carry a parity verdict
+    (rank 0 of a single process), every entry also carries a parity verdict
     from a sample through the CUDA path against the oracle."""
     sub = argparse.Namespace(**vars(args))
     sub.steps = max(1, min(args.steps, 20))
@@ -836,16 +982,20 @@ def other_workloads(args, dev, dist, ws, rank) -> dict:
     out["qgz_hierarchical"] = entry(
         line, qgz_parity_on_sample(wl.QGZ_HIERARCHICAL, 64, 2, dev) if check else None)
     torch.cuda.empty_cache()
-    line, _ = run_qgz(wl.QGZ_HIERARCHICAL, sub, dev, dist, ws, hop1_ef=True)
-    out["qgz_hier_ef"] = entry(line)
-    torch.cuda.empty_cache()
-    for ef in ("bf16", "int8"):
-        line, _ = run_qgz(wl.QGZ_SINGLE_HOP, sub, dev, dist, ws, ef=ef)
-        out[f"qgz_{ef}ef"] = entry(line)
+    for name, variant, runner, w in (
+            ("qgz_hier_ef", "hier_ef", lambda w: run_qgz(w, sub, dev, dist, ws, hop1_ef=True),
+             wl.QGZ_HIERARCHICAL),
+            ("qgz_hier_fused", "hier_fused", lambda w: run_qgz_hier_fused(w, sub, dev, dist, ws),
+             wl.QGZ_HIERARCHICAL),
+            ("qgz_bf16ef", "bf16ef", lambda w: run_qgz(w, sub, dev, dist, ws, ef="bf16"),
+             wl.QGZ_SINGLE_HOP),
+            ("qgz_int8ef", "int8ef", lambda w: run_qgz(w, sub, dev, dist, ws, ef="int8"),
+             wl.QGZ_SINGLE_HOP),
+            ("qgz_fused", "fused", lambda w: run_qgz_fused(w, sub, dev, dist, ws),
+             wl.QGZ_SINGLE_HOP)):
+        line, _ = runner(w)
         torch.cuda.empty_cache()
-    line, _ = run_qgz_fused(wl.QGZ_SINGLE_HOP, sub, dev, dist, ws)
-    out["qgz_fused"] = entry(line)
-    torch.cuda.empty_cache()
+        out[name] = entry(line, variant_parity_on_sample(w, variant, 64, 2, dev) if check else None)
     line, t = run_qwz(wl.QWZ_WEIGHTS, sub, dev, dist, ws)
     out["qwz"] = entry(line, qwz_parity(wl.QWZ_WEIGHTS, t, dev) if check else None)
     del t
@@ -1049,7 +1199,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
                     choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef",
-                             "qgz_hier_ef", "qgz_tiny", "qgz_hierarchical", "qwz", "sr", "all"])
+                             "qgz_hier_ef", "qgz_hier_fused", "qgz_tiny", "qgz_hierarchical",
+                             "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
@@ -1081,7 +1232,7 @@ def main(argv=None):
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
     names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef", "qgz_tiny",
-              "qgz_hierarchical", "qgz_hier_ef", "qwz", "sr"]
+              "qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qwz", "sr"]
              if args.workload == "all" else [args.workload])
     for name in names:
         if name == "qgz_hier_ef":
@@ -1093,6 +1244,10 @@ def main(argv=None):
         elif name == "qgz_fused":
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
             line, _ = run_qgz_fused(w, args, dev, dist, ws)
+        elif name == "qgz_hier_fused":
+            w = (wl.QGZ_HIERARCHICAL if args.scale == 1
+                 else qgz_sample(wl.QGZ_HIERARCHICAL, args.scale))
+            line, _ = run_qgz_hier_fused(w, args, dev, dist, ws)
         elif name in wl.QGZ_WORKLOADS:
             w = wl.QGZ_WORKLOADS[name]
             if args.scale > 1:

@@ -221,6 +221,33 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes,
                              void *out, int out_dtype, void *stream);
 
 /*
+ * wc_qgz_first_hop_fused -- the hierarchical step's first stage in one
+ * kernel: every rank's error-feedback quantization (wc_ef_quant_int4 with
+ * G groups) and the first, intra-group hop (wc_dequant_reduce_requant)
+ * together.  For every block of the first hop's output it runs
+ * wc_ef_quant_int4's arithmetic on the L ranks of the unit's group, in
+ * local-rank order, on the blocks those ranks send to the unit, and adds
+ * their dequantized values from +0 as the first hop does before
+ * requantizing; so out_codes, out_scales, ef, codes and scales are
+ * bit-identical to calling the two in sequence, while the ranks' codes are
+ * never read back from memory.  ("ZeROPlusPlus.md" §1.2: qgZ reduces
+ * intra-node first, with CUDA kernel fusion; with every rank in one GPU's
+ * memory the fusion can span the intra-group all-to-all.)  The second hop is
+ * wc_dequant_reduce with G groups on out_codes and out_scales.
+ * g, ef    : as wc_ef_quant_int4 (ef may be NULL).
+ * codes, scales : the ranks' send buffers as wc_ef_quant_int4 writes them,
+ *           or both NULL to skip writing them.
+ * out_codes, out_scales : the first hop's output, as
+ *           wc_dequant_reduce_requant writes it.
+ * Requires the sizes of wc_dequant_reduce_requant and B >= 128.
+ */
+WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
+                                  float *scales, int64_t N, int R, int G, int B,
+                                  float err_scale, float err_beta,
+                                  uint8_t *out_codes, float *out_scales,
+                                  void *stream);
+
+/*
  * wc_qwz_quant_int8 -- qwZ block weight quantization.
  * Per block of B weights (bf16 widened exactly to fp32), m = max |w|:
  *   m < 127 * 2^-126: scale = 0, q = 0

@@ -153,6 +153,27 @@ def test_fused_step_argument_errors(lib):
     assert call(N=0, g=None, out=None) == binding.WC_OK
 
 
+def test_fused_first_hop_argument_errors(lib):
+    f = lib.wc_qgz_first_hop_fused
+    ok = (FAKE, FAKE, FAKE, FAKE, 16 * 512, 8, 2, 256, 1.0, 0.5, FAKE, FAKE, None)
+    names = ["g", "ef", "codes", "scales", "N", "R", "G", "B", "s", "beta", "oc", "os", "st"]
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+    assert call(B=64) == binding.WC_EINVAL                 # below 128
+    assert call(G=3) == binding.WC_EINVAL                  # G must divide R
+    assert call(scales=None) == binding.WC_EINVAL          # scales without codes
+    assert call(oc=None) == binding.WC_EINVAL
+    assert call(os=MIS) == binding.WC_EALIGN
+    assert call(ef=MIS) == binding.WC_EALIGN
+    assert call(codes=MIS) == binding.WC_EALIGN
+    assert call(g=None) == binding.WC_EINVAL
+    assert call(N=1 << 31, R=2, G=2, B=512) == binding.WC_ERANGE  # G*N reaches 2^32
+    assert call(N=0, g=None, oc=None, os=None) == binding.WC_OK
+
+
 def test_bf16ef_and_replica_argument_errors(lib):
     f = lib.wc_ef_quant_int4_bf16ef
     assert f(FAKE, None, FAKE, FAKE, 1024, 4, 1, 256, 1.0, 0.5, None) == binding.WC_EINVAL

@@ -1,7 +1,7 @@
 """The default bench line's summary of the other configurations
 (`workloads`): every entry carries per-kernel times, algorithmic bytes and
-fractions, and the hierarchical, qwZ and SR entries a parity verdict from a
-sample through the CUDA path against the oracle.  Run here on small
+fractions, and a parity verdict from a sample through the CUDA path against
+the oracle.  Run here on small
 stand-ins of the workloads (same R, G, B and parameters, fewer elements)."""
 import argparse
 import dataclasses
@@ -26,11 +26,12 @@ def test_other_workloads_summary(monkeypatch):
                               no_overlap=True, no_cpu_baseline=False)
     dev = torch.device("cuda", 0)
     out = bench.other_workloads(args, dev, None, 1, 0)
-    assert set(out) == {"qgz_hierarchical", "qgz_hier_ef", "qgz_bf16ef", "qgz_int8ef",
-                        "qgz_fused", "qwz", "sr"}
+    assert set(out) == {"qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_bf16ef",
+                        "qgz_int8ef", "qgz_fused", "qwz", "sr"}
     want_kernels = {
         "qgz_hierarchical": {"ef_quant_int4", "dequant_reduce_requant", "dequant_reduce"},
         "qgz_hier_ef": {"ef_quant_int4", "dequant_reduce_requant", "dequant_reduce"},
+        "qgz_hier_fused": {"qgz_first_hop_fused", "dequant_reduce"},
         "qgz_bf16ef": {"ef_quant_int4", "dequant_reduce"},
         "qgz_int8ef": {"ef_quant_int4", "dequant_reduce"},
         "qgz_fused": {"qgz_step_fused"},
@@ -43,5 +44,5 @@ def test_other_workloads_summary(monkeypatch):
         for k in e["kernels"].values():
             assert k["ms"] > 0 and k["algorithmic_bytes"] > 0 and k["frac"] > 0
             assert set(k["ms_percentiles"]) == {"median", "p10", "p90"}
-    for name in ("qgz_hierarchical", "qwz", "sr"):
-        assert out[name]["parity"]["verdict"] == "bit-exact", (name, out[name]["parity"])
+    for name, e in out.items():
+        assert e["parity"]["verdict"] == "bit-exact", (name, e["parity"])

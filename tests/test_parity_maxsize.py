@@ -1,6 +1,7 @@
 """Parity at the largest sizes the ABI accepts, where 32-bit indexing ends.
 
-qgZ with R*N = 2^32 - 1024 (R = 2), qwZ with n = 2^32 - 2048 and SR with
+qgZ with R*N = 2^32 - 1024 (R = 2), the fused first hop with R*N = 2^32 - 8192
+(4 ranks in 2 groups), qwZ with n = 2^32 - 2048 and SR with
 n = 2^32 - 1 (its scalar tail included).  The oracle cannot run these sizes
 whole, so sampled blocks at the start and the very end of every rank,
 slice and shard are recomputed on the CPU as small problems of their own.
@@ -279,4 +280,53 @@ def test_packed_kernels_at_the_largest_size(dev):
         assert_bits_equal(to_host(e8[x0:x0 + B]), e8c, f"int8 error r={r} b={b}")
         assert_bits_equal(to_host(es[x0 // B:x0 // B + 1]), esc, f"int8 error scale r={r} b={b}")
     del g, e8, es, codes, scales
+    torch.cuda.empty_cache()
+
+
+def test_fused_first_hop_at_the_largest_size(dev):
+    """wc_qgz_first_hop_fused with R*N = 2^32 - 8192 (4 ranks in 2 groups,
+    B = 512).  Each sampled first-hop output block is one small problem: the
+    L ranks' error-feedback quantization of the blocks they send to the unit,
+    then a first hop of L sources with one block each.  About 27 GB of device
+    memory."""
+    R, G, B, s, beta = 4, 2, 512, 1.0, 0.5
+    L = R // G
+    N = (1 << 30) - R * B             # R*N = 2^32 - 8192; B divides N/R
+    S = N // R
+    g = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+    for r in range(R):
+        wl.draw_bf16(N, 1e-3, 7300 + r, dev, out=g[r])
+    gf = g.view(-1)
+    ef = torch.zeros(R * N, dtype=torch.float32, device=dev)
+    codes = torch.empty(R * N // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R * N // B, dtype=torch.float32, device=dev)
+    oc = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
+    os_ = torch.empty(G * N // B, dtype=torch.float32, device=dev)
+    binding.qgz_first_hop_fused(gf, ef, codes, scales, oc, os_, N, R, G, B, s, beta)
+    torch.cuda.synchronize()
+    for u in (0, R - 1):
+        grp, l = divmod(u, L)
+        for gq in (0, G - 1):
+            for j in (0, S // B - 1):
+                mc = np.zeros(L * L * B // 2, np.uint8)
+                ms = np.ones(L * L, np.float32)
+                for lq in range(L):
+                    r = grp * L + lq
+                    x0 = r * N + (gq * L + l) * S + j * B      # gradient order
+                    p0 = r * N + (l * G + gq) * S + j * B      # send position
+                    e_cpu = np.zeros(B, np.float32)
+                    cc, cs = ORC.ef_quant_int4(to_host(gf[x0:x0 + B]).copy(), e_cpu, B, 1, 1, B,
+                                               s, beta)
+                    where = f"rank {r} sub-slice {gq} block {j}"
+                    assert_bits_equal(to_host(codes[p0 // 2:(p0 + B) // 2]), cc, "codes " + where)
+                    assert_bits_equal(to_host(scales[p0 // B:p0 // B + 1]), cs, "scale " + where)
+                    assert_bits_equal(to_host(ef[x0:x0 + B]), e_cpu, "error " + where)
+                    mc[lq * L * B // 2:(lq * L * B + B) // 2] = cc
+                    ms[lq * L] = cs[0]
+                wc_, ws_ = ORC.dequant_reduce_requant(mc, ms, L * B, L, 1, B)
+                o0 = (u * G + gq) * S + j * B
+                where = f"unit {u} sub-slice {gq} block {j}"
+                assert_bits_equal(to_host(oc[o0 // 2:(o0 + B) // 2]), wc_[:B // 2], "codes " + where)
+                assert_bits_equal(to_host(os_[o0 // B:o0 // B + 1]), ws_[:1], "scale " + where)
+    del g, ef, codes, scales, oc, os_
     torch.cuda.empty_cache()

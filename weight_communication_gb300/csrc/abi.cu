@@ -209,6 +209,34 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes, float
                      fn);
 }
 
+WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                                  int64_t N, int R, int G, int B, float err_scale,
+                                  float err_beta, uint8_t *out_codes, float *out_scales,
+                                  void *stream) {
+    static const char *fn = "wc_qgz_first_hop_fused";
+    wc::QgzGeometry geo;
+    int rc = qgz_geometry(fn, N, R, G, B, &geo);
+    if (rc != WC_OK) return rc;
+    if (B < 128) return fail(WC_EINVAL, "%s: block B=%d must be at least 128", fn, B);
+    if (N * (int64_t)G >= (int64_t(1) << 32))
+        return fail(WC_ERANGE, "%s: G*N must be below 2^32", fn);
+    if ((codes == nullptr) != (scales == nullptr))
+        return fail(WC_EINVAL, "%s: codes and scales must both be given or both be NULL", fn);
+    if (N == 0) return WC_OK;
+    WC_REQUIRE_PTR(fn, g);
+    WC_REQUIRE_PTR(fn, out_codes);
+    WC_REQUIRE_PTR(fn, out_scales);
+    if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
+    if (codes != nullptr && (!aligned16(codes) || !aligned16(scales)))
+        return fail(WC_EALIGN, "%s: codes or scales is not 16-byte aligned", fn);
+    if (!aligned16(out_codes) || !aligned16(out_scales))
+        return fail(WC_EALIGN, "%s: out_codes or out_scales is not 16-byte aligned", fn);
+    return from_cuda(wc::launch_qgz_first_hop_fused(g, ef, codes, scales, geo, B, err_scale,
+                                                    err_beta, out_codes, out_scales,
+                                                    static_cast<cudaStream_t>(stream)),
+                     fn);
+}
+
 static int qwz_sizes(const char *fn, int64_t n, int B) {
     if (n < 0) return fail(WC_EINVAL, "%s: n = %lld is negative", fn, (long long)n);
     if (!pow2_in(B, 32, 4096))

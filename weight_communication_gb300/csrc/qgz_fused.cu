@@ -169,6 +169,194 @@ static cudaError_t launch_fused_b(const uint16_t *g, float *ef, uint8_t *codes, 
                                            out_bf16, stream);
 }
 
+// ---------------------------------------------------------------------------
+// The hierarchical first stage in one kernel: every rank's EF-quant fused
+// with the first (intra-group) hop
+// ---------------------------------------------------------------------------
+//
+// One warp per first-hop output block: unit u = g*L + l (grid z), sub-slice
+// g' (grid y), block j of the sub-slice (grid x).  The unit's sum takes, from
+// each local rank l' of group g (rank g*L + l'), block j of gradient slice
+// g'*L + l: the block that rank sends to local rank l for sub-slice g' (send
+// position l*G + g').  For l' = 0..L-1 in order the warp runs that rank's
+// error-feedback quantization of the block (the arithmetic of
+// wc_ef_quant_int4), writes its codes and scale at the send position when
+// asked to, and adds the dequantized values to the running fp32 sum (from
+// +0, in local-rank order); then it requantizes the sum to the first hop's
+// output (the arithmetic of wc_dequant_reduce_requant).  Every (rank, slice,
+// block) belongs to exactly one output block, so every gradient block is
+// quantized once, and the codes are never read back from memory.  The next
+// rank's block is loaded while the current one is processed.  Up to B = 512
+// a register budget for three CTAs of 256 threads per SM (80 registers, a
+// 12-byte spill with EF and codes) keeps more loads in flight than the
+// compiler's own choice of 122 registers: about 1 % faster at B = 512.
+template <int B, bool HAS_EF, bool WRITE_CODES>
+__global__ void __launch_bounds__(256, B <= 512 ? 3 : 1)
+qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
+                           uint8_t *__restrict__ codes, float *__restrict__ scales,
+                           QgzGeometry geo, float s, float beta, float one_minus_beta,
+                           uint8_t *__restrict__ out_codes, float *__restrict__ out_scales) {
+    static_assert(B >= 128 && B % 128 == 0, "one warp per block");
+    constexpr int K = B / 128;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const uint32_t off = (blockIdx.x * (blockDim.x / kWarp) + threadIdx.x / kWarp) * B;
+    if (off >= geo.S) return;  // whole warp: the grid's x is rounded up
+    const uint32_t gq = blockIdx.y, u = blockIdx.z;
+    const uint32_t grp = u / geo.L, l = u - grp * geo.L;
+    // local rank l' reads gradient elements xbase + l'*N + 128k + 4*lane and
+    // writes its codes at send position cbase + l'*N + ...
+    const uint32_t xbase = grp * geo.L * geo.N + (gq * geo.L + l) * geo.S + off;
+    const uint32_t cbase = grp * geo.L * geo.N + (l * geo.G + gq) * geo.S + off;
+    const uint32_t o0 = (u * geo.G + gq) * geo.S + off;  // first output of the block
+    const uint64_t total_out = uint64_t(geo.G) * geo.N;
+
+    float acc[K][4];
+    uint2 gv[K];
+    float4 ev[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[k][j] = 0.0f;
+        const uint32_t x = xbase + 128u * k + 4u * lane;  // local rank 0
+        gv[k] = make_uint2(0u, 0u);
+        ev[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
+            gv[k] = ld_stream_u2(g + x);
+            if (HAS_EF) ev[k] = ld_stream_f4(ef + x);
+        }
+    }
+
+    for (uint32_t lq = 0; lq < geo.L; ++lq) {
+        const uint32_t xr = xbase + lq * geo.N;
+        uint2 gn[K];
+        float4 en[K];
+        if (lq + 1 < geo.L) {  // prefetch the next local rank's block
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const uint32_t x = xr + geo.N + 128u * k + 4u * lane;
+                gn[k] = make_uint2(0u, 0u);
+                en[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total)) {
+                    gn[k] = ld_stream_u2(g + x);
+                    if (HAS_EF) en[k] = ld_stream_f4(ef + x);
+                }
+            }
+        }
+        float c[K][4];
+        float e[K][4];
+        float m = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const float gf[4] = {bf16_bits_to_f32(gv[k].x & 0xFFFFu), bf16_bits_to_f32(gv[k].x >> 16),
+                                 bf16_bits_to_f32(gv[k].y & 0xFFFFu), bf16_bits_to_f32(gv[k].y >> 16)};
+            e[k][0] = ev[k].x; e[k][1] = ev[k].y; e[k][2] = ev[k].z; e[k][3] = ev[k].w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                c[k][j] = HAS_EF ? __fadd_rn(gf[j], __fmul_rn(s, e[k][j])) : gf[j];
+                m = fmaxf(m, fabsf(c[k][j]));
+            }
+        }
+        m = group_max<kWarp>(m);
+        const BlockScale bs = block_scale<7>(m);
+        const uint32_t cr = cbase + lq * geo.N;  // this rank's send position
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const uint32_t x = xr + 128u * k + 4u * lane;
+            uint32_t packed = 0;
+            float4 eo;
+            float *o = &eo.x;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const QCode qc = quant_code<7>(c[k][j], bs);
+                const float d = dequant(qc.q, bs.scale);
+                acc[k][j] = __fadd_rn(acc[k][j], d);
+                if (WRITE_CODES) packed |= (qc.bits & 15u) << (4 * j);
+                if (HAS_EF)
+                    o[j] = __fadd_rn(__fmul_rn(beta, e[k][j]),
+                                     __fmul_rn(one_minus_beta, __fsub_rn(c[k][j], d)));
+            }
+            if (HAS_EF && WC_IN_BOUNDS(uint64_t(x) + 4 <= geo.total))
+                __stcs(reinterpret_cast<float4 *>(ef + x), eo);
+            const uint32_t pos = cr + 128u * k + 4u * lane;
+            if (WRITE_CODES && WC_IN_BOUNDS(uint64_t(pos) + 4 <= geo.total))
+                __stcs(reinterpret_cast<unsigned short *>(codes + pos / 2), (unsigned short)packed);
+        }
+        if (WRITE_CODES && lane == 0 && WC_IN_BOUNDS(cr / B < geo.total / B))
+            __stcs(scales + cr / B, bs.scale);
+        if (lq + 1 < geo.L) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                gv[k] = gn[k];
+                ev[k] = en[k];
+            }
+        }
+    }
+
+    // requantize the block's sums for the second hop
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = fmaxf(m, fabsf(acc[k][j]));
+    m = group_max<kWarp>(m);
+    const BlockScale bs = block_scale<7>(m);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) packed |= (quant_code<7>(acc[k][j], bs).bits & 15u) << (4 * j);
+        const uint32_t o = o0 + 128u * k + 4u * lane;
+        if (WC_IN_BOUNDS(uint64_t(o) + 4 <= total_out))
+            __stcs(reinterpret_cast<unsigned short *>(out_codes + o / 2), (unsigned short)packed);
+    }
+    if (lane == 0 && WC_IN_BOUNDS(uint64_t(o0 / B) < total_out / B)) __stcs(out_scales + o0 / B, bs.scale);
+}
+
+template <int B, bool HAS_EF, bool WRITE_CODES>
+static cudaError_t launch_first_hop_fused_3(const uint16_t *g, float *ef, uint8_t *codes,
+                                            float *scales, const QgzGeometry &geo, float s,
+                                            float beta, uint8_t *out_codes, float *out_scales,
+                                            cudaStream_t stream) {
+    const uint32_t threads = 256;
+    const uint32_t warps = geo.S / B;  // blocks per sub-slice
+    const dim3 grid((warps + threads / kWarp - 1) / (threads / kWarp), geo.G, geo.R);
+    qgz_first_hop_fused_kernel<B, HAS_EF, WRITE_CODES><<<grid, threads, 0, stream>>>(
+        g, ef, codes, scales, geo, s, beta, 1.0f - beta, out_codes, out_scales);
+    return cudaPeekAtLastError();
+}
+
+template <int B>
+static cudaError_t launch_first_hop_fused_b(const uint16_t *g, float *ef, uint8_t *codes,
+                                            float *scales, const QgzGeometry &geo, float s,
+                                            float beta, uint8_t *out_codes, float *out_scales,
+                                            cudaStream_t stream) {
+    if (ef) {
+        if (codes)
+            return launch_first_hop_fused_3<B, true, true>(g, ef, codes, scales, geo, s, beta,
+                                                           out_codes, out_scales, stream);
+        return launch_first_hop_fused_3<B, true, false>(g, ef, codes, scales, geo, s, beta,
+                                                        out_codes, out_scales, stream);
+    }
+    if (codes)
+        return launch_first_hop_fused_3<B, false, true>(g, ef, codes, scales, geo, s, beta,
+                                                        out_codes, out_scales, stream);
+    return launch_first_hop_fused_3<B, false, false>(g, ef, codes, scales, geo, s, beta,
+                                                     out_codes, out_scales, stream);
+}
+
+cudaError_t launch_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
+                                       float *scales, const QgzGeometry &geo, int B, float s,
+                                       float beta, uint8_t *out_codes, float *out_scales,
+                                       cudaStream_t stream) {
+    switch (B) {
+        case 128: return launch_first_hop_fused_b<128>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
+        case 256: return launch_first_hop_fused_b<256>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
+        case 512: return launch_first_hop_fused_b<512>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
+        case 1024: return launch_first_hop_fused_b<1024>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 WC_CHECK_RECORD_READER(check_record_qgz_fused)
 
 cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, float *scales,

@@ -37,6 +37,12 @@ cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, 
                                   const QgzGeometry &geo, int B, float s, float beta,
                                   float out_scale, void *out, bool out_bf16,
                                   cudaStream_t stream);
+// codes/scales: the ranks' send buffers, or both NULL; out_codes/out_scales:
+// the first hop's output, as launch_dequant_reduce_requant writes it.
+cudaError_t launch_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
+                                       float *scales, const QgzGeometry &geo, int B, float s,
+                                       float beta, uint8_t *out_codes, float *out_scales,
+                                       cudaStream_t stream);
 // replica: bf16 [n] written with the dequantized weights, or NULL.
 cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
                                   uint16_t *replica, uint32_t n, int B, cudaStream_t stream);
