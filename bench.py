@@ -203,6 +203,8 @@ KERNEL_SOURCES = {
                       "weight_communication_gb300/csrc/wc_device.cuh"],
     "qgz_step_fused": ["weight_communication_gb300/csrc/qgz_fused.cu",
                        "weight_communication_gb300/csrc/wc_device.cuh"],
+    "qgz_first_hop_fused": ["weight_communication_gb300/csrc/qgz_fused.cu",
+                            "weight_communication_gb300/csrc/wc_device.cuh"],
 }
 
 
@@ -596,7 +598,9 @@ def run_qgz_hier_fused(w: wl.QgzWorkload, args, dev, dist, ws):
             "roofline": {"bound": "hbm", "kernel": "qgz_first_hop_fused",
                          "achieved": kernels["qgz_first_hop_fused"]["GB/s"], "peak": peak,
                          "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
-                         "frac": kernels["qgz_first_hop_fused"]["frac"], "traffic": None,
+                         "frac": kernels["qgz_first_hop_fused"]["frac"],
+                         "traffic": ncu_traffic("qgz_first_hop_fused", "qgz_hierarchical",
+                                                w.R * w.N),
                          "algorithmic_bytes": kb["qgz_first_hop_fused"]},
             "kernels": kernels, "gpu_launches": 2 * args.steps, "clocks": clocks}, None
 
