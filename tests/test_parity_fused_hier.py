@@ -79,3 +79,71 @@ def test_first_hop_fused_then_second_hop(dev):
     want = ORC.dequant_reduce(oc1, os1, N, R, G, B, 1.0, True)
     assert_bits_equal(to_host(out), want, "two-hop shards")
     assert_bits_equal(to_host(ef_dev), ef_cpu, "error buffer")
+
+
+def _oracle_step(w, g, ef):
+    """The oracle's step: quantization of every rank, then the flat reduce or
+    the two hops; returns (shards, send codes, send scales, first-hop codes,
+    first-hop scales)."""
+    cc, cs = ORC.ef_quant_int4(g, ef, w.N, w.R, w.G, w.B, w.err_scale, w.err_beta)
+    if w.G > 1:
+        c1, s1 = ORC.dequant_reduce_requant(cc, cs, w.N, w.R, w.G, w.B)
+        return ORC.dequant_reduce(c1, s1, w.N, w.R, w.G, w.B, 1.0, w.out_bf16), cc, cs, c1, s1
+    return ORC.dequant_reduce(cc, cs, w.N, w.R, 1, w.B, 1.0, w.out_bf16), cc, cs, None, None
+
+
+@pytest.mark.parametrize("which", ["single_hop", "hierarchical"])
+def test_fused_reducer_matches_oracle(dev, which):
+    """QgzReducer(fused=True): three chained steps against the oracle --
+    shards, error buffer, send buffers and (hierarchical) the first hop's
+    output -- in one launch (flat) or two (hierarchical)."""
+    from weight_communication_gb300 import workloads as wl
+    from weight_communication_gb300.qgz import QgzReducer
+    w = (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 24) if which == "single_hop"
+         else wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 5))
+    out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+    red = QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype,
+                     device=dev, fused=True)
+    assert red.launches_per_step == (2 if w.G > 1 else 1)
+    ef = np.zeros(w.R * w.N, np.float32)
+    for t in range(3):
+        g = wl.qgz_gradients(w, t, device=dev)
+        out = red.step(g)
+        torch.cuda.synchronize()
+        want, cc, cs, c1, s1 = _oracle_step(w, to_host(g).ravel(), ef)
+        assert_bits_equal(to_host(out), want, f"{which} shards step {t}")
+        assert_bits_equal(to_host(red.ef), ef, f"{which} error buffer step {t}")
+        assert_bits_equal(to_host(red.codes), cc, f"{which} send codes step {t}")
+        assert_bits_equal(to_host(red.scales), cs, f"{which} send scales step {t}")
+        if w.G > 1:
+            assert_bits_equal(to_host(red.codes1), c1, f"first-hop codes step {t}")
+            assert_bits_equal(to_host(red.scales1), s1, f"first-hop scales step {t}")
+
+
+def test_fused_reducer_in_host_pipeline_and_graph(dev):
+    """A fused reducer in HostPipeline and in a replayed CUDA graph gives, step
+    after step, the shards and error buffer of unfused serial steps."""
+    from weight_communication_gb300 import workloads as wl
+    from weight_communication_gb300.qgz import GraphedStep, HostPipeline, QgzReducer
+    for w in (wl.QGZ_SINGLE_HOP.scaled(8 * 256 * 16), wl.QGZ_HIERARCHICAL.scaled(16 * 512 * 4)):
+        out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
+        view = torch.int16 if out_dtype == torch.bfloat16 else torch.int32
+
+        def make(fused):
+            return QgzReducer(w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, out_dtype=out_dtype,
+                              device=dev, fused=fused)
+        piped, graphed_red, serial = make(True), make(True), make(False)
+        steps = 4
+        g_host = [wl.qgz_gradients(w, t).pin_memory() for t in range(steps)]
+        out_host = [torch.empty(w.N, dtype=out_dtype).pin_memory() for _ in range(steps)]
+        HostPipeline(piped).run(g_host, out_host)
+        graphed = GraphedStep(graphed_red)
+        for t in range(steps):
+            graphed.g.copy_(g_host[t].view(-1).to(dev))
+            got = graphed.replay().clone()
+            want = serial.step(g_host[t].to(dev).view(-1))
+            torch.cuda.synchronize()
+            assert torch.equal(got.view(view), want.view(view)), (w.name, "graph", t)
+            assert torch.equal(out_host[t].view(view), want.cpu().view(view)), (w.name, "host", t)
+        for red in (piped, graphed_red):
+            assert torch.equal(red.ef.view(torch.int32), serial.ef.view(torch.int32)), w.name

@@ -1,0 +1,29 @@
+"""Host-side checks of QgzReducer's options (no GPU): the fused step's
+preconditions and the launch count it reports."""
+import pytest
+import torch
+
+from weight_communication_gb300.qgz import DevicePipeline, QgzReducer
+
+
+def test_fused_step_preconditions():
+    kw = dict(N=8 * 256, R=8, G=1, B=256, device="cpu")
+    with pytest.raises(ValueError, match="fp32 error buffer"):
+        QgzReducer(**kw, ef_dtype=torch.bfloat16, fused=True)
+    with pytest.raises(ValueError, match="fp32 error buffer"):
+        QgzReducer(**kw, ef_dtype=torch.int8, fused=True)
+    with pytest.raises(ValueError, match="B >= 128"):
+        QgzReducer(N=8 * 64, R=8, G=1, B=64, device="cpu", fused=True)
+    with pytest.raises(ValueError, match="first-hop error buffer"):
+        QgzReducer(N=16 * 512, R=16, G=2, B=512, device="cpu", hop1_ef=True, fused=True)
+    assert QgzReducer(**kw, fused=True).launches_per_step == 1
+    assert QgzReducer(**kw, use_ef=False, fused=True).launches_per_step == 1
+    assert QgzReducer(N=16 * 512, R=16, G=2, B=512, device="cpu", fused=True).launches_per_step == 2
+    assert QgzReducer(**kw).launches_per_step == 2
+    assert QgzReducer(N=16 * 512, R=16, G=2, B=512, device="cpu").launches_per_step == 3
+
+
+def test_device_pipeline_refuses_a_fused_reducer():
+    red = QgzReducer(N=8 * 256, R=8, G=1, B=256, device="cpu", fused=True)
+    with pytest.raises(ValueError, match="no separate reduce"):
+        DevicePipeline(red)

@@ -10,7 +10,9 @@ memory and no extra time.
 
 `QgzReducer` owns the device buffers of one problem (error feedback, send
 buffers, first-hop buffers, reduced shards) and runs a step as 2 launches
-(flat) or 3 launches (hierarchical) on one stream.  `DevicePipeline` overlaps
+(flat) or 3 launches (hierarchical) on one stream, or, with `fused=True`, as
+1 launch (flat: wc_qgz_step_fused) or 2 (hierarchical: wc_qgz_first_hop_fused,
+then the second hop), bit for bit the same.  `DevicePipeline` overlaps
 each step's reduce with the next quantization, `HostPipeline` runs steps from
 and to host memory with the copies overlapped, and `GraphedStep` replays a
 step captured in a CUDA graph.
@@ -35,13 +37,16 @@ class QgzReducer:
     def __init__(self, N: int, R: int, G: int = 1, B: int = 256, err_scale: float = 1.0,
                  err_beta: float = 0.0, use_ef: bool = True, out_dtype=torch.float32,
                  out_scale: float = 1.0, device="cuda", ef_dtype=torch.float32,
-                 hop1_ef: bool = False):
+                 hop1_ef: bool = False, fused: bool = False):
         """ef_dtype: torch.float32, torch.bfloat16 for the half-size error
         buffer (wc_ef_quant_int4_bf16ef), or torch.int8 for the quarter-size
         one (wc_ef_quant_int4_int8ef: int8 codes in self.ef, one fp32 scale per
         block in self.ef_scales).  hop1_ef (G > 1): keep an fp32 error
         for the first hop's requantization too (wc_dequant_reduce_requant_ef),
-        with the same err_scale and err_beta."""
+        with the same err_scale and err_beta.  fused: step() quantizes and
+        reduces (flat) or quantizes and runs the first hop (hierarchical) in
+        one kernel, still writing the send buffers; it takes an fp32 error
+        buffer or none, no first-hop error buffer, and B >= 128."""
         self.N, self.R, self.G, self.B = N, R, G, B
         self.err_scale, self.err_beta = err_scale, err_beta
         self.out_scale = out_scale
@@ -61,9 +66,19 @@ class QgzReducer:
             self.codes1 = self.scales1 = None
         self.ef1 = torch.zeros(G * N, dtype=torch.float32, device=dev) if (hop1_ef and G > 1) else None
         self.out = torch.empty(N, dtype=out_dtype, device=dev)
+        if fused:
+            if ef_dtype != torch.float32:
+                raise ValueError("fused steps take an fp32 error buffer (or none)")
+            if self.ef1 is not None:
+                raise ValueError("fused steps take no first-hop error buffer")
+            if B < 128:
+                raise ValueError(f"fused steps need B >= 128 (one warp per block), got B={B}")
+        self.fused = fused
 
     @property
     def launches_per_step(self) -> int:
+        if self.fused:
+            return 2 if self.G > 1 else 1
         return 3 if self.G > 1 else 2
 
     def quantize(self, g: torch.Tensor, stream=None, send=None) -> None:
@@ -112,11 +127,32 @@ class QgzReducer:
             self.reduce_first_hop(stream)
         return self.reduce_last_hop(stream)
 
-    def step(self, g: torch.Tensor, stream=None) -> torch.Tensor:
+    def step(self, g: torch.Tensor, stream=None, out: torch.Tensor | None = None) -> torch.Tensor:
         """Quantize every rank's gradient g ([R, N] bf16 on the device) and
-        reduce; returns the [N] reduced shards (destination-major)."""
+        reduce; returns the [N] reduced shards (destination-major), in
+        self.out unless `out` is given."""
+        if self.fused:
+            return self.step_fused(g, stream, out)
         self.quantize(g, stream)
-        return self.reduce(stream)
+        if self.G > 1:
+            self.reduce_first_hop(stream)
+        return self.reduce_last_hop(stream, out=out)
+
+    def step_fused(self, g: torch.Tensor, stream=None,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+        """The step in the fused kernels: flat, one launch that quantizes every
+        rank and reduces every shard; hierarchical, one launch that quantizes
+        every rank and runs the first hop, then the second hop."""
+        out = self.out if out is None else out
+        if self.G > 1:
+            binding.qgz_first_hop_fused(g.reshape(-1), self.ef, self.codes, self.scales,
+                                        self.codes1, self.scales1, self.N, self.R, self.G,
+                                        self.B, self.err_scale, self.err_beta, stream)
+            return self.reduce_last_hop(stream, out=out)
+        binding.qgz_step_fused(g.reshape(-1), self.ef, self.codes, self.scales, out, self.N,
+                               self.R, self.B, self.err_scale, self.err_beta, self.out_scale,
+                               stream)
+        return out
 
     def step_host(self, g_host: torch.Tensor, g_dev: torch.Tensor, out_host: torch.Tensor,
                   stream: torch.cuda.Stream | None = None) -> torch.Tensor:
@@ -145,6 +181,9 @@ class DevicePipeline:
     """
 
     def __init__(self, red: QgzReducer):
+        if red.fused:
+            raise ValueError("a fused step has no separate reduce to overlap; "
+                             "use QgzReducer.step or HostPipeline")
         self.red = red
         self.send = [(red.codes, red.scales),
                      (torch.empty_like(red.codes), torch.empty_like(red.scales))]
@@ -224,13 +263,20 @@ class HostPipeline:
                 self.g_loaded[b].record(self.h2d)
             with torch.cuda.stream(self.comp):
                 self.comp.wait_event(self.g_loaded[b])
-                red.quantize(self.g_dev[b], self.comp)
-                self.g_consumed[b].record(self.comp)
-                if self._started[b]:
-                    self.comp.wait_event(self.out_copied[b])
-                if red.G > 1:
-                    red.reduce_first_hop(self.comp)
-                red.reduce_last_hop(self.comp, out=self.out_dev[b])
+                if red.fused:
+                    # the fused launch writes the shards while it reads g
+                    if self._started[b]:
+                        self.comp.wait_event(self.out_copied[b])
+                    red.step_fused(self.g_dev[b], self.comp, out=self.out_dev[b])
+                    self.g_consumed[b].record(self.comp)
+                else:
+                    red.quantize(self.g_dev[b], self.comp)
+                    self.g_consumed[b].record(self.comp)
+                    if self._started[b]:
+                        self.comp.wait_event(self.out_copied[b])
+                    if red.G > 1:
+                        red.reduce_first_hop(self.comp)
+                    red.reduce_last_hop(self.comp, out=self.out_dev[b])
                 self.out_ready[b].record(self.comp)
             with torch.cuda.stream(self.d2h):
                 self.d2h.wait_event(self.out_ready[b])
@@ -240,8 +286,8 @@ class HostPipeline:
 
 
 class GraphedStep:
-    """One QgzReducer step captured in a CUDA graph: replay() issues its two
-    or three kernels with a single graph launch, which takes the host's
+    """One QgzReducer step captured in a CUDA graph: replay() issues its one
+    to three kernels with a single graph launch, which takes the host's
     per-call work (argument checks, marshalling, one launch per kernel) off
     the step.  That matters when the step is short: a small problem is
     bound by how fast the host can launch, not by the GPU.
