@@ -147,3 +147,36 @@ def test_fused_reducer_in_host_pipeline_and_graph(dev):
             assert torch.equal(out_host[t].view(view), want.cpu().view(view)), (w.name, "host", t)
         for red in (piped, graphed_red):
             assert torch.equal(red.ef.view(torch.int32), serial.ef.view(torch.int32)), w.name
+
+
+def test_fused_first_hop_stays_inside_its_buffers(dev):
+    """Guard regions around every output of the fused first stage stay
+    untouched, and a zero-size call writes nothing."""
+    R, G, B = 6, 3, 128
+    N = R * B * 5
+    pad = 4096
+    g = edge_gradients(R, N, B, seed=98)
+    efd = torch.full((R * N + 2 * pad,), 13.0, dtype=torch.float32, device=dev)
+    efd[pad:pad + R * N] = 0.0
+    codes = torch.full((R * N // 2 + 2 * pad,), 0xA5, dtype=torch.uint8, device=dev)
+    scales = torch.full((R * N // B + 2 * pad,), -5.0, dtype=torch.float32, device=dev)
+    c1 = torch.full((G * N // 2 + 2 * pad,), 0x5A, dtype=torch.uint8, device=dev)
+    s1 = torch.full((G * N // B + 2 * pad,), -9.0, dtype=torch.float32, device=dev)
+    binding.qgz_first_hop_fused(to_dev(g, dev), efd[pad:pad + R * N], codes[pad:pad + R * N // 2],
+                                scales[pad:pad + R * N // B], c1[pad:pad + G * N // 2],
+                                s1[pad:pad + G * N // B], N, R, G, B, 1.0, 0.5)
+    torch.cuda.synchronize()
+    for t, fill, n in ((efd, 13.0, R * N), (codes, 0xA5, R * N // 2), (scales, -5.0, R * N // B),
+                       (c1, 0x5A, G * N // 2), (s1, -9.0, G * N // B)):
+        assert bool((t[:pad] == fill).all()) and bool((t[pad + n:] == fill).all())
+    ef_cpu = np.zeros(R * N, np.float32)
+    cc, cs = ORC.ef_quant_int4(g, ef_cpu, N, R, G, B, 1.0, 0.5)
+    oc1, os1 = ORC.dequant_reduce_requant(cc, cs, N, R, G, B)
+    assert_bits_equal(to_host(c1[pad:pad + G * N // 2]), oc1, "first-hop codes")
+    assert_bits_equal(to_host(s1[pad:pad + G * N // B]), os1, "first-hop scales")
+    empty_u8 = torch.empty(0, dtype=torch.uint8, device=dev)
+    empty_f = torch.empty(0, dtype=torch.float32, device=dev)
+    binding.qgz_first_hop_fused(torch.empty(0, dtype=torch.bfloat16, device=dev), None, None, None,
+                                empty_u8, empty_f, 0, 4, 2, 256)
+    torch.cuda.synchronize()
+    assert bool((c1[:pad] == 0x5A).all())
