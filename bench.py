@@ -9,12 +9,13 @@ per second (R*N per step) through both kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload qgz_single_hop|qgz_fused|qgz_bf16ef|qgz_int8ef|qgz_hier_ef|
-                                qgz_hier_fused|qgz_tiny|qgz_hierarchical|qwz|sr|all]
+                                qgz_hier_fused|qgz_hier_ef_fused|qgz_tiny|qgz_hierarchical|
+                                qwz|sr|all]
 
 The other workloads: the same step as one fused kernel (qgz_fused), with a
 bf16 or an int8 error buffer (qgz_bf16ef, qgz_int8ef), the 16-rank two-hop reduce without and with
 first-hop error feedback (qgz_hierarchical, qgz_hier_ef), the same with its
-first stage as one kernel (qgz_hier_fused), the L2-resident
+first stage as one kernel (qgz_hier_fused, qgz_hier_ef_fused), the L2-resident
 4-rank step (qgz_tiny), the qwZ int8 round trip and one-pass replica (qwz),
 and the bf16 stochastic-rounding accumulate (sr).
 
@@ -205,6 +206,8 @@ KERNEL_SOURCES = {
                        "weight_communication_gb300/csrc/wc_device.cuh"],
     "qgz_first_hop_fused": ["weight_communication_gb300/csrc/qgz_fused.cu",
                             "weight_communication_gb300/csrc/wc_device.cuh"],
+    "qgz_first_hop_fused_ef1": ["weight_communication_gb300/csrc/qgz_fused.cu",
+                                "weight_communication_gb300/csrc/wc_device.cuh"],
 }
 
 
@@ -537,13 +540,15 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
             "gpu_launches": args.steps, "clocks": clocks}, None
 
 
-def run_qgz_hier_fused(w: wl.QgzWorkload, args, dev, dist, ws):
+def run_qgz_hier_fused(w: wl.QgzWorkload, args, dev, dist, ws, hop1_ef: bool = False):
     """The hierarchical step with its first stage as one kernel (every rank's
     EF-quant fused with the first hop, writing the error buffers, the send
-    buffers and the first hop's output), then the second hop."""
+    buffers and the first hop's output; with hop1_ef the first hop also keeps
+    its own error buffer), then the second hop."""
     from weight_communication_gb300 import binding
     assert w.G > 1
     ef = torch.zeros(w.R * w.N, dtype=torch.float32, device=dev)
+    ef1 = torch.zeros(w.G * w.N, dtype=torch.float32, device=dev) if hop1_ef else None
     codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
     scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
     c1 = torch.empty(w.G * w.N // 2, dtype=torch.uint8, device=dev)
@@ -558,7 +563,8 @@ def run_qgz_hier_fused(w: wl.QgzWorkload, args, dev, dist, ws):
             if timer is not None:
                 timer.mark(ti, 0)
             binding.qgz_first_hop_fused(batches[i % nbatch].view(-1), ef, codes, scales, c1, s1,
-                                        w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, stream)
+                                        w.N, w.R, w.G, w.B, w.err_scale, w.err_beta, stream,
+                                        ef1=ef1)
             if timer is not None:
                 timer.mark(ti, 1)
             binding.dequant_reduce(c1, s1, out, w.N, w.R, w.G, w.B, 1.0, stream)
@@ -582,24 +588,27 @@ def run_qgz_hier_fused(w: wl.QgzWorkload, args, dev, dist, ws):
     pct = timer.per_kernel_percentiles()
     peak, kind = measured_peaks()
     kb = {"qgz_first_hop_fused": int(w.R * w.N * (2 + 8 + 0.5) + w.R * w.N // w.B * 4
-                                     + w.G * w.N * (0.5 + 4 / w.B)),
+                                     + w.G * w.N * (0.5 + 4 / w.B + (8 if hop1_ef else 0))),
           "dequant_reduce": int(w.N * (w.G * (0.5 + 4 / w.B) + (2 if w.out_bf16 else 4)))}
     kernels = {n: {"ms": round(per[n], 5), "ms_percentiles": pct[n], "algorithmic_bytes": kb[n],
                    "GB/s": round(kb[n] / (per[n] / 1e3) / 1e9, 1),
                    "frac": round(kb[n] / (per[n] / 1e3) / 1e9 / peak, 4)} for n in names}
-    return {"metric": METRIC + " [hierarchical, fused first stage]",
+    tag = "fused first stage with first-hop EF" if hop1_ef else "fused first stage"
+    return {"metric": METRIC + f" [hierarchical, {tag}]",
             "value": job_throughput(w.R * w.N, ws, ms), "unit": "elements/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded normal gradients with sparse outliers)",
-            "config": {"workload": w.name + " fused first stage", "R": w.R, "N": w.N, "G": w.G,
+            "config": {"workload": f"{w.name} {tag}", "R": w.R, "N": w.N, "G": w.G,
                        "B": w.B, "err_scale": w.err_scale, "err_beta": w.err_beta,
+                       "ef1": "fp32" if hop1_ef else None,
                        "l2": f"inputs exceed L2 ({w.R * w.N * 10 / 1e9:.1f} GB per step)"},
             "roofline": {"bound": "hbm", "kernel": "qgz_first_hop_fused",
                          "achieved": kernels["qgz_first_hop_fused"]["GB/s"], "peak": peak,
                          "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
                          "frac": kernels["qgz_first_hop_fused"]["frac"],
-                         "traffic": ncu_traffic("qgz_first_hop_fused", "qgz_hierarchical",
+                         "traffic": ncu_traffic("qgz_first_hop_fused_ef1" if hop1_ef
+                                                else "qgz_first_hop_fused", "qgz_hierarchical",
                                                 w.R * w.N),
                          "algorithmic_bytes": kb["qgz_first_hop_fused"]},
             "kernels": kernels, "gpu_launches": 2 * args.steps, "clocks": clocks}, None
@@ -840,7 +849,8 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
       int8ef     -- the step with an int8 error buffer and a scale per block
       fused      -- the flat step as one kernel (wc_qgz_step_fused)
       hier_fused -- the two-hop step with its first stage as one kernel
-                    (wc_qgz_first_hop_fused), then the second hop"""
+                    (wc_qgz_first_hop_fused), then the second hop
+      hier_ef_fused -- the same with the first hop's own error buffer"""
     import oracle
     from weight_communication_gb300 import binding
     from weight_communication_gb300.qgz import QgzReducer
@@ -856,7 +866,7 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
         bufs["ef_scales"] = np.zeros(R * N // B, np.float32)
     else:
         bufs["ef"] = np.zeros(R * N, np.float32)
-    if variant == "hier_ef":
+    if variant in ("hier_ef", "hier_ef_fused"):
         bufs["ef1"] = np.zeros(G * N, np.float32)
     for _ in range(steps):
         if variant == "bf16ef":
@@ -873,8 +883,10 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
     out_dtype = torch.bfloat16 if sw.out_bf16 else torch.float32
     gd = wl.from_u16(g, dev)
     got = {}
-    if variant in ("fused", "hier_fused"):
+    if variant in ("fused", "hier_fused", "hier_ef_fused"):
         ef = torch.zeros(R * N, dtype=torch.float32, device=dev)
+        ef1 = (torch.zeros(G * N, dtype=torch.float32, device=dev)
+               if variant == "hier_ef_fused" else None)
         out = torch.empty(N, dtype=out_dtype, device=dev)
         c1 = torch.empty(G * N // 2, dtype=torch.uint8, device=dev)
         s1 = torch.empty(G * N // B, dtype=torch.float32, device=dev)
@@ -882,9 +894,12 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
             if variant == "fused":
                 binding.qgz_step_fused(gd, ef, None, None, out, N, R, B, s, beta)
             else:
-                binding.qgz_first_hop_fused(gd, ef, None, None, c1, s1, N, R, G, B, s, beta)
+                binding.qgz_first_hop_fused(gd, ef, None, None, c1, s1, N, R, G, B, s, beta,
+                                            ef1=ef1)
                 binding.dequant_reduce(c1, s1, out, N, R, G, B)
         got["ef"] = ef
+        if ef1 is not None:
+            got["ef1"] = ef1
     else:
         ef_dtype = {"bf16ef": torch.bfloat16, "int8ef": torch.int8}.get(variant, torch.float32)
         red = QgzReducer(N, R, G, B, s, beta, out_dtype=out_dtype, device=dev,
@@ -990,6 +1005,9 @@ def other_workloads(args, dev, dist, ws, rank) -> dict:
             ("qgz_hier_ef", "hier_ef", lambda w: run_qgz(w, sub, dev, dist, ws, hop1_ef=True),
              wl.QGZ_HIERARCHICAL),
             ("qgz_hier_fused", "hier_fused", lambda w: run_qgz_hier_fused(w, sub, dev, dist, ws),
+             wl.QGZ_HIERARCHICAL),
+            ("qgz_hier_ef_fused", "hier_ef_fused",
+             lambda w: run_qgz_hier_fused(w, sub, dev, dist, ws, hop1_ef=True),
              wl.QGZ_HIERARCHICAL),
             ("qgz_bf16ef", "bf16ef", lambda w: run_qgz(w, sub, dev, dist, ws, ef="bf16"),
              wl.QGZ_SINGLE_HOP),
@@ -1203,8 +1221,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
                     choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef",
-                             "qgz_hier_ef", "qgz_hier_fused", "qgz_tiny", "qgz_hierarchical",
-                             "qwz", "sr", "all"])
+                             "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused", "qgz_tiny",
+                             "qgz_hierarchical", "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-overlap", action="store_true",
@@ -1236,7 +1254,8 @@ def main(argv=None):
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
     names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef", "qgz_tiny",
-              "qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qwz", "sr"]
+              "qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused", "qwz",
+              "sr"]
              if args.workload == "all" else [args.workload])
     for name in names:
         if name == "qgz_hier_ef":
@@ -1248,10 +1267,11 @@ def main(argv=None):
         elif name == "qgz_fused":
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
             line, _ = run_qgz_fused(w, args, dev, dist, ws)
-        elif name == "qgz_hier_fused":
+        elif name in ("qgz_hier_fused", "qgz_hier_ef_fused"):
             w = (wl.QGZ_HIERARCHICAL if args.scale == 1
                  else qgz_sample(wl.QGZ_HIERARCHICAL, args.scale))
-            line, _ = run_qgz_hier_fused(w, args, dev, dist, ws)
+            line, _ = run_qgz_hier_fused(w, args, dev, dist, ws,
+                                         hop1_ef=name == "qgz_hier_ef_fused")
         elif name in wl.QGZ_WORKLOADS:
             w = wl.QGZ_WORKLOADS[name]
             if args.scale > 1:

@@ -239,13 +239,19 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes,
  *           or both NULL to skip writing them.
  * out_codes, out_scales : the first hop's output, as
  *           wc_dequant_reduce_requant writes it.
- * Requires the sizes of wc_dequant_reduce_requant and B >= 128.
+ * ef1      : NULL, or the first hop's own error buffer [G*N] fp32 (in
+ *           place, output order), applied to the requantization as
+ *           wc_dequant_reduce_requant_ef does, with the same err_scale and
+ *           err_beta as the ranks' buffers ("Merge LoCo with Zero++",
+ *           review thread: the inter-node message's error buffer).
+ * Requires the sizes of wc_dequant_reduce_requant and B >= 128; every
+ * pointer 16-byte aligned.
  */
 WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
                                   float *scales, int64_t N, int R, int G, int B,
                                   float err_scale, float err_beta,
                                   uint8_t *out_codes, float *out_scales,
-                                  void *stream);
+                                  float *ef1, void *stream);
 
 /*
  * wc_qwz_quant_int8 -- qwZ block weight quantization.

@@ -155,8 +155,9 @@ def test_fused_step_argument_errors(lib):
 
 def test_fused_first_hop_argument_errors(lib):
     f = lib.wc_qgz_first_hop_fused
-    ok = (FAKE, FAKE, FAKE, FAKE, 16 * 512, 8, 2, 256, 1.0, 0.5, FAKE, FAKE, None)
-    names = ["g", "ef", "codes", "scales", "N", "R", "G", "B", "s", "beta", "oc", "os", "st"]
+    ok = (FAKE, FAKE, FAKE, FAKE, 16 * 512, 8, 2, 256, 1.0, 0.5, FAKE, FAKE, None, None)
+    names = ["g", "ef", "codes", "scales", "N", "R", "G", "B", "s", "beta", "oc", "os", "ef1",
+             "st"]
     def call(**kw):
         a = list(ok)
         for k, v in kw.items():
@@ -169,6 +170,7 @@ def test_fused_first_hop_argument_errors(lib):
     assert call(os=MIS) == binding.WC_EALIGN
     assert call(ef=MIS) == binding.WC_EALIGN
     assert call(codes=MIS) == binding.WC_EALIGN
+    assert call(ef1=MIS) == binding.WC_EALIGN
     assert call(g=None) == binding.WC_EINVAL
     assert call(N=1 << 31, R=2, G=2, B=512) == binding.WC_ERANGE  # G*N reaches 2^32
     assert call(N=0, g=None, oc=None, os=None) == binding.WC_OK

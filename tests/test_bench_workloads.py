@@ -26,12 +26,13 @@ def test_other_workloads_summary(monkeypatch):
                               no_overlap=True, no_cpu_baseline=False)
     dev = torch.device("cuda", 0)
     out = bench.other_workloads(args, dev, None, 1, 0)
-    assert set(out) == {"qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_bf16ef",
-                        "qgz_int8ef", "qgz_fused", "qwz", "sr"}
+    assert set(out) == {"qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused",
+                        "qgz_bf16ef", "qgz_int8ef", "qgz_fused", "qwz", "sr"}
     want_kernels = {
         "qgz_hierarchical": {"ef_quant_int4", "dequant_reduce_requant", "dequant_reduce"},
         "qgz_hier_ef": {"ef_quant_int4", "dequant_reduce_requant", "dequant_reduce"},
         "qgz_hier_fused": {"qgz_first_hop_fused", "dequant_reduce"},
+        "qgz_hier_ef_fused": {"qgz_first_hop_fused", "dequant_reduce"},
         "qgz_bf16ef": {"ef_quant_int4", "dequant_reduce"},
         "qgz_int8ef": {"ef_quant_int4", "dequant_reduce"},
         "qgz_fused": {"qgz_step_fused"},

@@ -8,7 +8,8 @@ of k blocks. It also draws an error buffer (none, fp32, bf16 or int8),
 first-hop error feedback, the output type, the output scale and LoCo's s and
 beta. It then runs three chained steps through QgzReducer, so every
 combination of the kernels' fixed and general forms meets the others.  The
-flat cases also run the fused single-kernel step.  The send buffers, the
+flat cases also run the fused single-kernel step, and draws with B >= 128
+and an fp32 error buffer (or none) run through the fused reducer.  The send buffers, the
 first-hop buffers, the error buffers and the shards must all equal the
 oracle's composition of the same steps ("ZeRO++", qgZ; "Merge LoCo with
 Zero++", Overview)."""
@@ -112,12 +113,37 @@ def _describe(seed: int) -> str:
 
 @pytest.mark.parametrize("seed", SEEDS, ids=[_describe(s) for s in SEEDS])
 def test_random_geometry_chained_steps(dev, seed):
+    _chained_steps(dev, seed, fused=False)
+
+
+def _reducer_fusable(geo: dict) -> bool:
+    """QgzReducer(fused=True) takes B >= 128 and an fp32 error buffer or none,
+    flat or hierarchical, with or without the first hop's error buffer."""
+    return geo["B"] >= 128 and geo["ef"] in (None, torch.float32)
+
+
+REDUCER_FUSED_SEEDS = ([s for s in range(2000) if _reducer_fusable(draw_geometry(s))
+                        and draw_geometry(s)["G"] > 1][:32]
+                       + [s for s in range(2000) if _reducer_fusable(draw_geometry(s))
+                          and draw_geometry(s)["G"] == 1][:8])
+
+
+@pytest.mark.parametrize("seed", REDUCER_FUSED_SEEDS,
+                         ids=[_describe(s) for s in REDUCER_FUSED_SEEDS])
+def test_random_geometry_fused_reducer(dev, seed):
+    """The same chained steps through QgzReducer(fused=True): the flat step
+    as one kernel, or the hierarchical first stage (with the first hop's
+    error buffer when drawn) as one kernel, then the second hop."""
+    _chained_steps(dev, seed, fused=True)
+
+
+def _chained_steps(dev, seed, fused):
     geo = draw_geometry(seed)
     R, N, G, B = geo["R"], geo["N"], geo["G"], geo["B"]
     red = QgzReducer(N, R, G, B, geo["s"], geo["beta"], use_ef=geo["ef"] is not None,
                      out_dtype=torch.bfloat16 if geo["out_bf16"] else torch.float32,
                      out_scale=geo["out_scale"], device=dev,
-                     ef_dtype=geo["ef"] or torch.float32, hop1_ef=geo["hop1_ef"])
+                     ef_dtype=geo["ef"] or torch.float32, hop1_ef=geo["hop1_ef"], fused=fused)
     orc = OracleSteps(geo)
     for t in range(3):
         g = gradients(geo, seed, t)

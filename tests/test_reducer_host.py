@@ -14,8 +14,8 @@ def test_fused_step_preconditions():
         QgzReducer(**kw, ef_dtype=torch.int8, fused=True)
     with pytest.raises(ValueError, match="B >= 128"):
         QgzReducer(N=8 * 64, R=8, G=1, B=64, device="cpu", fused=True)
-    with pytest.raises(ValueError, match="first-hop error buffer"):
-        QgzReducer(N=16 * 512, R=16, G=2, B=512, device="cpu", hop1_ef=True, fused=True)
+    red = QgzReducer(N=16 * 512, R=16, G=2, B=512, device="cpu", hop1_ef=True, fused=True)
+    assert red.ef1 is not None and red.launches_per_step == 2
     assert QgzReducer(**kw, fused=True).launches_per_step == 1
     assert QgzReducer(**kw, use_ef=False, fused=True).launches_per_step == 1
     assert QgzReducer(N=16 * 512, R=16, G=2, B=512, device="cpu", fused=True).launches_per_step == 2

@@ -32,7 +32,7 @@ SIGNATURES = {
     "wc_dequant_reduce_requant": [_P, _P, _I64, _I, _I, _I, _P, _P, _P],
     "wc_dequant_reduce_requant_ef": [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F, _P],
     "wc_qgz_step_fused": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
-    "wc_qgz_first_hop_fused": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P, _P, _P],
+    "wc_qgz_first_hop_fused": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P, _P, _P, _P],
     "wc_ef_quant_int4_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_ef_quant_int4_int8ef": [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
@@ -218,17 +218,20 @@ def qgz_step_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor
 def qgz_first_hop_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor | None,
                         scales: torch.Tensor | None, out_codes: torch.Tensor,
                         out_scales: torch.Tensor, N: int, R: int, G: int, B: int,
-                        err_scale: float = 1.0, err_beta: float = 0.0, stream=None) -> None:
+                        err_scale: float = 1.0, err_beta: float = 0.0, stream=None,
+                        ef1: torch.Tensor | None = None) -> None:
     """wc_qgz_first_hop_fused: every rank's EF-quant and the first hop in one
     kernel.  codes/scales (the send buffers) may both be None to skip writing
-    them; out_codes/out_scales receive the first hop's output."""
+    them; out_codes/out_scales receive the first hop's output; ef1 (fp32
+    [G*N], or None) is the first hop's own error buffer."""
     d = g.device
     _call(d, "wc_qgz_first_hop_fused", _dev(g, "g", torch.bfloat16, R * N, d),
           _dev(ef, "ef", torch.float32, R * N, d),
           _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
           _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),
-          _dev(out_scales, "out_scales", torch.float32, G * N // B, d), _stream(g, stream))
+          _dev(out_scales, "out_scales", torch.float32, G * N // B, d),
+          _dev(ef1, "ef1", torch.float32, G * N, d), _stream(g, stream))
 
 
 def qwz_quant_int8(w: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, B: int,

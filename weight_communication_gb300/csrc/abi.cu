@@ -212,7 +212,7 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes, float
 WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
                                   int64_t N, int R, int G, int B, float err_scale,
                                   float err_beta, uint8_t *out_codes, float *out_scales,
-                                  void *stream) {
+                                  float *ef1, void *stream) {
     static const char *fn = "wc_qgz_first_hop_fused";
     wc::QgzGeometry geo;
     int rc = qgz_geometry(fn, N, R, G, B, &geo);
@@ -231,8 +231,9 @@ WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes, 
         return fail(WC_EALIGN, "%s: codes or scales is not 16-byte aligned", fn);
     if (!aligned16(out_codes) || !aligned16(out_scales))
         return fail(WC_EALIGN, "%s: out_codes or out_scales is not 16-byte aligned", fn);
+    if (ef1 != nullptr && !aligned16(ef1)) return fail(WC_EALIGN, "%s: ef1 is not 16-byte aligned", fn);
     return from_cuda(wc::launch_qgz_first_hop_fused(g, ef, codes, scales, geo, B, err_scale,
-                                                    err_beta, out_codes, out_scales,
+                                                    err_beta, out_codes, out_scales, ef1,
                                                     static_cast<cudaStream_t>(stream)),
                      fn);
 }

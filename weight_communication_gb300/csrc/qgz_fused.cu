@@ -183,19 +183,22 @@ static cudaError_t launch_fused_b(const uint16_t *g, float *ef, uint8_t *codes, 
 // wc_ef_quant_int4), writes its codes and scale at the send position when
 // asked to, and adds the dequantized values to the running fp32 sum (from
 // +0, in local-rank order); then it requantizes the sum to the first hop's
-// output (the arithmetic of wc_dequant_reduce_requant).  Every (rank, slice,
+// output (the arithmetic of wc_dequant_reduce_requant, or with HAS_EF1 that
+// of wc_dequant_reduce_requant_ef: the sum compensated with the first hop's
+// own error buffer, which is then updated).  Every (rank, slice,
 // block) belongs to exactly one output block, so every gradient block is
 // quantized once, and the codes are never read back from memory.  The next
 // rank's block is loaded while the current one is processed.  Up to B = 512
 // a register budget for three CTAs of 256 threads per SM (80 registers, a
 // 12-byte spill with EF and codes) keeps more loads in flight than the
 // compiler's own choice of 122 registers: about 1 % faster at B = 512.
-template <int B, bool HAS_EF, bool WRITE_CODES>
+template <int B, bool HAS_EF, bool WRITE_CODES, bool HAS_EF1>
 __global__ void __launch_bounds__(256, B <= 512 ? 3 : 1)
 qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, float *__restrict__ ef,
                            uint8_t *__restrict__ codes, float *__restrict__ scales,
                            QgzGeometry geo, float s, float beta, float one_minus_beta,
-                           uint8_t *__restrict__ out_codes, float *__restrict__ out_scales) {
+                           uint8_t *__restrict__ out_codes, float *__restrict__ out_scales,
+                           float *__restrict__ ef1) {
     static_assert(B >= 128 && B % 128 == 0, "one warp per block");
     constexpr int K = B / 128;
     const int lane = threadIdx.x & (kWarp - 1);
@@ -292,7 +295,20 @@ qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, float *__restrict__ e
         }
     }
 
-    // requantize the block's sums for the second hop
+    // requantize the block's sums for the second hop (compensated with the
+    // first hop's error buffer, in output order, when it has one)
+    float e1[K][4];
+    if (HAS_EF1) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const uint32_t o = o0 + 128u * k + 4u * lane;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (WC_IN_BOUNDS(uint64_t(o) + 4 <= total_out)) v = ld_stream_f4(ef1 + o);
+            e1[k][0] = v.x; e1[k][1] = v.y; e1[k][2] = v.z; e1[k][3] = v.w;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[k][j] = __fadd_rn(acc[k][j], __fmul_rn(s, e1[k][j]));
+        }
+    }
     float m = 0.0f;
 #pragma unroll
     for (int k = 0; k < K; ++k)
@@ -303,56 +319,78 @@ qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, float *__restrict__ e
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         uint32_t packed = 0;
+        float4 eo;
+        float *eout = &eo.x;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) packed |= (quant_code<7>(acc[k][j], bs).bits & 15u) << (4 * j);
+        for (int j = 0; j < 4; ++j) {
+            const QCode qc = quant_code<7>(acc[k][j], bs);
+            packed |= (qc.bits & 15u) << (4 * j);
+            if (HAS_EF1)
+                eout[j] = __fadd_rn(__fmul_rn(beta, e1[k][j]),
+                                    __fmul_rn(one_minus_beta,
+                                              __fsub_rn(acc[k][j], dequant(qc.q, bs.scale))));
+        }
         const uint32_t o = o0 + 128u * k + 4u * lane;
-        if (WC_IN_BOUNDS(uint64_t(o) + 4 <= total_out))
-            __stcs(reinterpret_cast<unsigned short *>(out_codes + o / 2), (unsigned short)packed);
+        if (!WC_IN_BOUNDS(uint64_t(o) + 4 <= total_out)) continue;
+        __stcs(reinterpret_cast<unsigned short *>(out_codes + o / 2), (unsigned short)packed);
+        if (HAS_EF1) __stcs(reinterpret_cast<float4 *>(ef1 + o), eo);
     }
     if (lane == 0 && WC_IN_BOUNDS(uint64_t(o0 / B) < total_out / B)) __stcs(out_scales + o0 / B, bs.scale);
+}
+
+template <int B, bool HAS_EF, bool WRITE_CODES, bool HAS_EF1>
+static cudaError_t launch_first_hop_fused_4(const uint16_t *g, float *ef, uint8_t *codes,
+                                            float *scales, const QgzGeometry &geo, float s,
+                                            float beta, uint8_t *out_codes, float *out_scales,
+                                            float *ef1, cudaStream_t stream) {
+    const uint32_t threads = 256;
+    const uint32_t warps = geo.S / B;  // blocks per sub-slice
+    const dim3 grid((warps + threads / kWarp - 1) / (threads / kWarp), geo.G, geo.R);
+    qgz_first_hop_fused_kernel<B, HAS_EF, WRITE_CODES, HAS_EF1><<<grid, threads, 0, stream>>>(
+        g, ef, codes, scales, geo, s, beta, 1.0f - beta, out_codes, out_scales, ef1);
+    return cudaPeekAtLastError();
 }
 
 template <int B, bool HAS_EF, bool WRITE_CODES>
 static cudaError_t launch_first_hop_fused_3(const uint16_t *g, float *ef, uint8_t *codes,
                                             float *scales, const QgzGeometry &geo, float s,
                                             float beta, uint8_t *out_codes, float *out_scales,
-                                            cudaStream_t stream) {
-    const uint32_t threads = 256;
-    const uint32_t warps = geo.S / B;  // blocks per sub-slice
-    const dim3 grid((warps + threads / kWarp - 1) / (threads / kWarp), geo.G, geo.R);
-    qgz_first_hop_fused_kernel<B, HAS_EF, WRITE_CODES><<<grid, threads, 0, stream>>>(
-        g, ef, codes, scales, geo, s, beta, 1.0f - beta, out_codes, out_scales);
-    return cudaPeekAtLastError();
+                                            float *ef1, cudaStream_t stream) {
+    if (ef1)
+        return launch_first_hop_fused_4<B, HAS_EF, WRITE_CODES, true>(
+            g, ef, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+    return launch_first_hop_fused_4<B, HAS_EF, WRITE_CODES, false>(
+        g, ef, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
 }
 
 template <int B>
 static cudaError_t launch_first_hop_fused_b(const uint16_t *g, float *ef, uint8_t *codes,
                                             float *scales, const QgzGeometry &geo, float s,
                                             float beta, uint8_t *out_codes, float *out_scales,
-                                            cudaStream_t stream) {
+                                            float *ef1, cudaStream_t stream) {
     if (ef) {
         if (codes)
             return launch_first_hop_fused_3<B, true, true>(g, ef, codes, scales, geo, s, beta,
-                                                           out_codes, out_scales, stream);
+                                                           out_codes, out_scales, ef1, stream);
         return launch_first_hop_fused_3<B, true, false>(g, ef, codes, scales, geo, s, beta,
-                                                        out_codes, out_scales, stream);
+                                                        out_codes, out_scales, ef1, stream);
     }
     if (codes)
         return launch_first_hop_fused_3<B, false, true>(g, ef, codes, scales, geo, s, beta,
-                                                        out_codes, out_scales, stream);
+                                                        out_codes, out_scales, ef1, stream);
     return launch_first_hop_fused_3<B, false, false>(g, ef, codes, scales, geo, s, beta,
-                                                     out_codes, out_scales, stream);
+                                                     out_codes, out_scales, ef1, stream);
 }
 
 cudaError_t launch_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
                                        float *scales, const QgzGeometry &geo, int B, float s,
                                        float beta, uint8_t *out_codes, float *out_scales,
-                                       cudaStream_t stream) {
+                                       float *ef1, cudaStream_t stream) {
     switch (B) {
-        case 128: return launch_first_hop_fused_b<128>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
-        case 256: return launch_first_hop_fused_b<256>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
-        case 512: return launch_first_hop_fused_b<512>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
-        case 1024: return launch_first_hop_fused_b<1024>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, stream);
+        case 128: return launch_first_hop_fused_b<128>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+        case 256: return launch_first_hop_fused_b<256>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+        case 512: return launch_first_hop_fused_b<512>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+        case 1024: return launch_first_hop_fused_b<1024>(g, ef, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
         default: return cudaErrorInvalidValue;
     }
 }

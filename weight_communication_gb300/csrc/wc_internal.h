@@ -42,7 +42,7 @@ cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, 
 cudaError_t launch_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
                                        float *scales, const QgzGeometry &geo, int B, float s,
                                        float beta, uint8_t *out_codes, float *out_scales,
-                                       cudaStream_t stream);
+                                       float *ef1, cudaStream_t stream);
 // replica: bf16 [n] written with the dequantized weights, or NULL.
 cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
                                   uint16_t *replica, uint32_t n, int B, cudaStream_t stream);

@@ -44,9 +44,9 @@ class QgzReducer:
         block in self.ef_scales).  hop1_ef (G > 1): keep an fp32 error
         for the first hop's requantization too (wc_dequant_reduce_requant_ef),
         with the same err_scale and err_beta.  fused: step() quantizes and
-        reduces (flat) or quantizes and runs the first hop (hierarchical) in
-        one kernel, still writing the send buffers; it takes an fp32 error
-        buffer or none, no first-hop error buffer, and B >= 128."""
+        reduces (flat) or quantizes and runs the first hop, with its error
+        buffer if any (hierarchical), in one kernel, still writing the send
+        buffers; it takes an fp32 error buffer or none, and B >= 128."""
         self.N, self.R, self.G, self.B = N, R, G, B
         self.err_scale, self.err_beta = err_scale, err_beta
         self.out_scale = out_scale
@@ -69,8 +69,6 @@ class QgzReducer:
         if fused:
             if ef_dtype != torch.float32:
                 raise ValueError("fused steps take an fp32 error buffer (or none)")
-            if self.ef1 is not None:
-                raise ValueError("fused steps take no first-hop error buffer")
             if B < 128:
                 raise ValueError(f"fused steps need B >= 128 (one warp per block), got B={B}")
         self.fused = fused
@@ -142,12 +140,14 @@ class QgzReducer:
                    out: torch.Tensor | None = None) -> torch.Tensor:
         """The step in the fused kernels: flat, one launch that quantizes every
         rank and reduces every shard; hierarchical, one launch that quantizes
-        every rank and runs the first hop, then the second hop."""
+        every rank and runs the first hop (with its error buffer, if the
+        reducer keeps one), then the second hop."""
         out = self.out if out is None else out
         if self.G > 1:
             binding.qgz_first_hop_fused(g.reshape(-1), self.ef, self.codes, self.scales,
                                         self.codes1, self.scales1, self.N, self.R, self.G,
-                                        self.B, self.err_scale, self.err_beta, stream)
+                                        self.B, self.err_scale, self.err_beta, stream,
+                                        ef1=self.ef1)
             return self.reduce_last_hop(stream, out=out)
         binding.qgz_step_fused(g.reshape(-1), self.ef, self.codes, self.scales, out, self.N,
                                self.R, self.B, self.err_scale, self.err_beta, self.out_scale,
