@@ -46,7 +46,9 @@ enum EfMode { kEfNone = 0, kEfF32 = 1, kEfBf16 = 2, kEfInt8 = 3 };
 // gives, bit for bit.  Lane t holds elements 128k + 4t + j of the block as
 // pairs (j = 0, 1) and (2, 3); the block's loads (gv: bf16 gradients, e8w:
 // stored error codes, es: stored error scale) are already in registers.
-template <int B>
+// S1: the error scale s is 1, so s*e is e itself (exact for every finite e,
+// signed zeros included) and its multiply is left out.
+template <int B, bool S1>
 __device__ __forceinline__ void int8ef_block(const uint2 (&gv)[B / 128],
                                              const uint32_t (&e8w)[B / 128], float es,
                                              int8_t *__restrict__ ef8,
@@ -71,7 +73,7 @@ __device__ __forceinline__ void int8ef_block(const uint2 (&gv)[B / 128],
             e[k][h] = ops.mul(ops.add(f, unbias8), es2);  // stored error: code (exact) * scale
             const uint32_t gw = h ? gv[k].y : gv[k].x;
             const f32x2 gf = pack2(__uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u));
-            c[k][h] = ops.add(gf, ops.mul(s2, e[k][h]));
+            c[k][h] = ops.add(gf, S1 ? e[k][h] : ops.mul(s2, e[k][h]));
             float a, b;
             unpack2(c[k][h], a, b);
             m = max3(m, fabsf(a), fabsf(b));
@@ -134,7 +136,7 @@ __device__ __forceinline__ void int8ef_block(const uint2 (&gv)[B / 128],
 // back to back: one block per warp under a budget of 8 CTAs per SM 0.388 ms,
 // two blocks with 4 CTAs 0.367-0.380 ms, three blocks with 3 CTAs 0.353 ms,
 // four blocks with 2 or 3 CTAs 0.365 ms.
-template <int B, int NB, int MINB>
+template <int B, int NB, int MINB, bool S1>
 __global__ void __launch_bounds__(256, MINB)
 ef_quant_int8ef_kernel(const uint16_t *__restrict__ g, int8_t *__restrict__ ef8,
                        float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
@@ -180,12 +182,12 @@ ef_quant_int8ef_kernel(const uint16_t *__restrict__ g, int8_t *__restrict__ ef8,
         if (off0 + b * B >= geo.S) break;
         const uint32_t tile0 = r * geo.N + slice * geo.S + off0 + b * B;
         const uint32_t out0 = r * geo.N + p * geo.S + off0 + b * B;
-        int8ef_block<B>(gv[b], e8w[b], es[b], ef8, ef_scales, codes, scales, geo, tile0, out0,
+        int8ef_block<B, S1>(gv[b], e8w[b], es[b], ef8, ef_scales, codes, scales, geo, tile0, out0,
                         lane, s, beta, one_minus_beta, ops);
     }
 }
 
-template <int B, int EF>
+template <int B, int EF, bool S1 = false>
 __device__ __forceinline__ void ef_quant_int4_warp(const uint16_t *__restrict__ g,
                                                    void *__restrict__ ef_v,
                                                    float *__restrict__ ef_scales,
@@ -268,7 +270,8 @@ __device__ __forceinline__ void ef_quant_int4_warp(const uint16_t *__restrict__ 
         e[k][0] = ev.x; e[k][1] = ev.y; e[k][2] = ev.z; e[k][3] = ev.w;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            c[k][j] = HAS_EF ? __fadd_rn(gf[j], __fmul_rn(s, e[k][j])) : gf[j];
+            // S1: s = 1, and s*e is e itself (exact for every finite e)
+            c[k][j] = HAS_EF ? __fadd_rn(gf[j], S1 ? e[k][j] : __fmul_rn(s, e[k][j])) : gf[j];
     }
 
     float m = 0.0f;
@@ -359,14 +362,16 @@ ef_quant_int4_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
 // instead of 4, so a warp has fewer bytes in flight; at B = 128 and 256 the
 // same code under a register budget for 8 CTAs (64 warps) per SM keeps more
 // of them resident.  (The fp32 buffer already saturates DRAM at 6 CTAs per
-// SM, and larger blocks would spill.)
-template <int B, int EF>
+// SM, and larger blocks would spill.)  S1: the error scale s is 1 (the
+// multiply by s is left out).
+template <int B, int EF, bool S1>
 __global__ void __launch_bounds__(256, 8)
 ef_quant_int4_resident8_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef_v,
                                float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
                                float *__restrict__ scales, QgzGeometry geo, float s, float beta,
                                float one_minus_beta) {
-    ef_quant_int4_warp<B, EF>(g, ef_v, ef_scales, codes, scales, geo, s, beta, one_minus_beta);
+    ef_quant_int4_warp<B, EF, S1>(g, ef_v, ef_scales, codes, scales, geo, s, beta,
+                                  one_minus_beta);
 }
 
 template <int B>
@@ -387,24 +392,45 @@ static cudaError_t launch_ef_quant_b(const uint16_t *g, void *ef, int ef_mode, f
     }
     const float omb = 1.0f - beta;
     constexpr bool kResident8 = B == 128 || B == 256;
-    if (ef != nullptr && ef_mode == kEfInt8 && B >= 128) {
-        // three blocks per warp at B = 128 and 256 (see ef_quant_int8ef_kernel)
-        constexpr int NB = kResident8 ? 3 : 1;
-        const uint32_t warps = (geo.S / B + NB - 1) / NB;
-        const dim3 g8((warps + threads / kWarp - 1) / (threads / kWarp), geo.R, geo.R);
-        ef_quant_int8ef_kernel<(B >= 128 ? B : 128), NB, (kResident8 ? 3 : 1)>
-            <<<g8, threads, 0, stream>>>(g, static_cast<int8_t *>(ef), ef_scales, codes, scales,
-                                         geo, s, beta, omb, exact2_constants());
-        return cudaPeekAtLastError();
+    if constexpr (B >= 128) {
+        if (ef != nullptr && ef_mode == kEfInt8) {
+            // three blocks per warp at B = 128 and 256 (see ef_quant_int8ef_kernel)
+            constexpr int NB = kResident8 ? 3 : 1;
+            const uint32_t warps = (geo.S / B + NB - 1) / NB;
+            const dim3 g8((warps + threads / kWarp - 1) / (threads / kWarp), geo.R, geo.R);
+            constexpr int MINB = kResident8 ? 3 : 1;
+            if (s == 1.0f)
+                ef_quant_int8ef_kernel<B, NB, MINB, true><<<g8, threads, 0, stream>>>(
+                    g, static_cast<int8_t *>(ef), ef_scales, codes, scales, geo, s, beta, omb,
+                    exact2_constants());
+            else
+                ef_quant_int8ef_kernel<B, NB, MINB, false><<<g8, threads, 0, stream>>>(
+                    g, static_cast<int8_t *>(ef), ef_scales, codes, scales, geo, s, beta, omb,
+                    exact2_constants());
+            return cudaPeekAtLastError();
+        }
     }
 #define WC_EFQ(KERNEL, MODE)                                                                   \
     KERNEL<B, MODE><<<grid, threads, 0, stream>>>(g, ef, ef_scales, codes, scales, geo, s, beta, \
                                                    omb)
-    if (ef == nullptr) WC_EFQ(ef_quant_int4_kernel, kEfNone);
-    else if (ef_mode == kEfBf16 && kResident8) WC_EFQ(ef_quant_int4_resident8_kernel, kEfBf16);
-    else if (ef_mode == kEfBf16) WC_EFQ(ef_quant_int4_kernel, kEfBf16);
-    else if (ef_mode == kEfInt8) WC_EFQ(ef_quant_int4_kernel, kEfInt8);
-    else WC_EFQ(ef_quant_int4_kernel, kEfF32);
+    if (ef == nullptr) {
+        WC_EFQ(ef_quant_int4_kernel, kEfNone);
+    } else if (ef_mode == kEfBf16) {
+        if constexpr (kResident8) {
+            if (s == 1.0f)
+                ef_quant_int4_resident8_kernel<B, kEfBf16, true><<<grid, threads, 0, stream>>>(
+                    g, ef, ef_scales, codes, scales, geo, s, beta, omb);
+            else
+                ef_quant_int4_resident8_kernel<B, kEfBf16, false><<<grid, threads, 0, stream>>>(
+                    g, ef, ef_scales, codes, scales, geo, s, beta, omb);
+        } else {
+            WC_EFQ(ef_quant_int4_kernel, kEfBf16);
+        }
+    } else if (ef_mode == kEfInt8) {
+        WC_EFQ(ef_quant_int4_kernel, kEfInt8);
+    } else {
+        WC_EFQ(ef_quant_int4_kernel, kEfF32);
+    }
 #undef WC_EFQ
     return cudaPeekAtLastError();
 }
