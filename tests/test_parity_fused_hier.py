@@ -1,8 +1,11 @@
 """Parity of wc_qgz_first_hop_fused -- every rank's EF-quant fused with the
 first (intra-group) hop -- against the oracle's composition of the two steps
-(orc_ef_quant_int4 with G groups, then orc_dequant_reduce_requant), bit for
-bit, over chained steps: the first hop's codes and scales, the error buffer,
-and, when written, the ranks' send buffers.
+(orc_ef_quant_int4 with G groups, then orc_dequant_reduce_requant, or
+orc_dequant_reduce_requant_ef with the first hop's own error buffer), bit for
+bit, over chained steps: the first hop's codes and scales, the error buffers,
+and, when written, the ranks' send buffers.  Also QgzReducer(fused=True),
+alone, in HostPipeline and in a replayed CUDA graph, guard regions around
+every output, and a zero-size call.
 
 "ZeROPlusPlus.md", §1.2 ZeRO++ (qgZ: intra-node reduce first, kernel fusion);
 "Merge LoCo with Zero++", Overview (error feedback before quantization)."""

@@ -1,6 +1,8 @@
-// qgz_fused.cu -- the whole flat qgZ step in one kernel: error-feedback
+// qgz_fused.cu -- the whole flat qgZ step in one kernel (error-feedback
 // compensation and int4 quantization of every rank, and the full-precision
-// reduce of every destination, without the codes round-tripping through HBM.
+// reduce of every destination), and the hierarchical step's first stage in
+// one kernel (the same quantization fused with the intra-group reduce and its
+// requantization), without the codes round-tripping through HBM.
 //
 // "ZeROPlusPlus.md", §1.2 ZeRO++ (quantized gradient communication): block
 // int4 quantization, all-to-all, full-precision reduce, and CUDA kernel
