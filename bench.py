@@ -9,11 +9,12 @@ per second (R*N per step) through both kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload qgz_single_hop|qgz_fused|qgz_bf16ef|qgz_int8ef|qgz_hier_ef|
-                                qgz_hier_fused|qgz_hier_ef_fused|qgz_tiny|qgz_hierarchical|
-                                qwz|sr|all]
+                                qgz_hier_fused|qgz_hier_ef_fused|qgz_bf16ef_fused|
+                                qgz_int8ef_fused|qgz_tiny|qgz_hierarchical|qwz|sr|all]
 
 The other workloads: the same step as one fused kernel (qgz_fused), with a
-bf16 or an int8 error buffer (qgz_bf16ef, qgz_int8ef), the 16-rank two-hop reduce without and with
+bf16 or an int8 error buffer (qgz_bf16ef, qgz_int8ef; fused: qgz_bf16ef_fused,
+qgz_int8ef_fused), the 16-rank two-hop reduce without and with
 first-hop error feedback (qgz_hierarchical, qgz_hier_ef), the same with its
 first stage as one kernel (qgz_hier_fused, qgz_hier_ef_fused), the L2-resident
 4-rank step (qgz_tiny), the qwZ int8 round trip and one-pass replica (qwz),
@@ -481,13 +482,20 @@ def run_qgz(w: wl.QgzWorkload, args, dev, dist, ws, ef: str = "fp32", hop1_ef: b
     return line, batches[0]
 
 
-def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
+EF_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "int8": torch.int8}
+EF_BYTES = {"fp32": 4, "bf16": 2, "int8": 1}     # per element, each way
+
+
+def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws, ef_kind: str = "fp32"):
     """The flat step as one fused launch (EF-quant of every rank + reduce),
-    writing the error buffers, the send buffers and the shards."""
+    writing the error buffers (fp32, bf16, or int8 with block scales), the
+    send buffers and the shards."""
     from weight_communication_gb300 import binding
     assert w.G == 1
     out_dtype = torch.bfloat16 if w.out_bf16 else torch.float32
-    ef = torch.zeros(w.R * w.N, dtype=torch.float32, device=dev)
+    ef = torch.zeros(w.R * w.N, dtype=EF_DTYPES[ef_kind], device=dev)
+    ef_scales = (torch.zeros(w.R * w.N // w.B, dtype=torch.float32, device=dev)
+                 if ef_kind == "int8" else None)
     codes = torch.empty(w.R * w.N // 2, dtype=torch.uint8, device=dev)
     scales = torch.empty(w.R * w.N // w.B, dtype=torch.float32, device=dev)
     out = torch.empty(w.N, dtype=out_dtype, device=dev)
@@ -498,7 +506,8 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
     with torch.cuda.stream(stream):
         def step(i):
             binding.qgz_step_fused(batches[i % nbatch].view(-1), ef, codes, scales, out, w.N,
-                                   w.R, w.B, w.err_scale, w.err_beta, 1.0, stream)
+                                   w.R, w.B, w.err_scale, w.err_beta, 1.0, stream,
+                                   ef_scales=ef_scales)
         for i in range(args.warmup):
             step(i)
         torch.cuda.synchronize(dev)
@@ -516,20 +525,25 @@ def run_qgz_fused(w: wl.QgzWorkload, args, dev, dist, ws):
     clocks = sampler.stop(t0, t1) if sampler else None
     ms = max_over_ranks(timer.step_sum_ms(), dist, dev)
     peak, kind = measured_peaks()
-    b = w.R * w.N * (2 + 4 + 4 + 0.5) + w.R * w.N // w.B * 4 + w.N * (2 if w.out_bf16 else 4)
+    eb = EF_BYTES[ef_kind]
+    b = (w.R * w.N * (2 + 2 * eb + 0.5) + w.R * w.N // w.B * (12 if ef_kind == "int8" else 4)
+         + w.N * (2 if w.out_bf16 else 4))
     achieved = b / (ms / 1e3) / 1e9
-    return {"metric": METRIC + " [fused single kernel]", "value": job_throughput(w.R * w.N, ws, ms),
+    tag = "fused single kernel" + ("" if ef_kind == "fp32" else f", {ef_kind} error buffer")
+    return {"metric": METRIC + f" [{tag}]", "value": job_throughput(w.R * w.N, ws, ms),
             "unit": "elements/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded normal gradients with sparse outliers)",
-            "config": {"workload": w.name + " fused", "R": w.R, "N": w.N, "G": 1, "B": w.B,
+            "config": {"workload": w.name + (" fused" if ef_kind == "fp32"
+                                             else f" fused {ef_kind} error buffer"),
+                       "R": w.R, "N": w.N, "G": 1, "B": w.B, "ef": ef_kind,
                        "err_scale": w.err_scale, "err_beta": w.err_beta,
-                       "l2": f"inputs exceed L2 ({w.R * w.N * 10 / 1e9:.1f} GB per step)"},
+                       "l2": f"inputs exceed L2 ({b / 1e9:.1f} GB per step)"},
             "roofline": {"bound": "hbm", "kernel": "qgz_step_fused", "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": f"hbm_gbs of {kind}", "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
-                         "traffic": ncu_traffic("qgz_step_fused", "qgz_single_hop", w.R * w.N)
-                         if "qgz_step_fused" in KERNEL_SOURCES else None,
+                         "traffic": (ncu_traffic("qgz_step_fused", "qgz_single_hop", w.R * w.N)
+                                     if ef_kind == "fp32" else None),
                          "algorithmic_bytes": int(b)},
             "kernels": {"qgz_step_fused": {"ms": round(ms, 5),
                                            "ms_percentiles": timer.per_kernel_percentiles()[
@@ -850,7 +864,9 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
       fused      -- the flat step as one kernel (wc_qgz_step_fused)
       hier_fused -- the two-hop step with its first stage as one kernel
                     (wc_qgz_first_hop_fused), then the second hop
-      hier_ef_fused -- the same with the first hop's own error buffer"""
+      hier_ef_fused -- the same with the first hop's own error buffer
+      bf16ef_fused, int8ef_fused -- the flat fused step with the bf16 or int8
+                    error buffer"""
     import oracle
     from weight_communication_gb300 import binding
     from weight_communication_gb300.qgz import QgzReducer
@@ -859,9 +875,9 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
     N, R, G, B, s, beta = sw.N, sw.R, sw.G, sw.B, sw.err_scale, sw.err_beta
     g = wl.as_u16(wl.qgz_gradients(sw, 0)).ravel().copy()
     bufs = {}                                     # oracle error buffers by name
-    if variant == "bf16ef":
+    if variant in ("bf16ef", "bf16ef_fused"):
         bufs["ef"] = np.zeros(R * N, np.uint16)
-    elif variant == "int8ef":
+    elif variant in ("int8ef", "int8ef_fused"):
         bufs["ef"] = np.zeros(R * N, np.int8)
         bufs["ef_scales"] = np.zeros(R * N // B, np.float32)
     else:
@@ -869,9 +885,9 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
     if variant in ("hier_ef", "hier_ef_fused"):
         bufs["ef1"] = np.zeros(G * N, np.float32)
     for _ in range(steps):
-        if variant == "bf16ef":
+        if variant in ("bf16ef", "bf16ef_fused"):
             codes, scales = orc.ef_quant_int4_bf16ef(g, bufs["ef"], N, R, G, B, s, beta)
-        elif variant == "int8ef":
+        elif variant in ("int8ef", "int8ef_fused"):
             codes, scales = orc.ef_quant_int4_int8ef(g, bufs["ef"], bufs["ef_scales"], N, R, G,
                                                      B, s, beta)
         else:
@@ -883,7 +899,18 @@ def variant_parity_on_sample(w: wl.QgzWorkload, variant: str, fraction: int, ste
     out_dtype = torch.bfloat16 if sw.out_bf16 else torch.float32
     gd = wl.from_u16(g, dev)
     got = {}
-    if variant in ("fused", "hier_fused", "hier_ef_fused"):
+    if variant in ("bf16ef_fused", "int8ef_fused"):
+        kind = variant[:4]
+        ef = torch.zeros(R * N, dtype=EF_DTYPES[kind], device=dev)
+        ef_scales = (torch.zeros(R * N // B, dtype=torch.float32, device=dev)
+                     if kind == "int8" else None)
+        out = torch.empty(N, dtype=out_dtype, device=dev)
+        for _ in range(steps):
+            binding.qgz_step_fused(gd, ef, None, None, out, N, R, B, s, beta, ef_scales=ef_scales)
+        got["ef"] = ef
+        if ef_scales is not None:
+            got["ef_scales"] = ef_scales
+    elif variant in ("fused", "hier_fused", "hier_ef_fused"):
         ef = torch.zeros(R * N, dtype=torch.float32, device=dev)
         ef1 = (torch.zeros(G * N, dtype=torch.float32, device=dev)
                if variant == "hier_ef_fused" else None)
@@ -1014,7 +1041,11 @@ def other_workloads(args, dev, dist, ws, rank) -> dict:
             ("qgz_int8ef", "int8ef", lambda w: run_qgz(w, sub, dev, dist, ws, ef="int8"),
              wl.QGZ_SINGLE_HOP),
             ("qgz_fused", "fused", lambda w: run_qgz_fused(w, sub, dev, dist, ws),
-             wl.QGZ_SINGLE_HOP)):
+             wl.QGZ_SINGLE_HOP),
+            ("qgz_bf16ef_fused", "bf16ef_fused",
+             lambda w: run_qgz_fused(w, sub, dev, dist, ws, ef_kind="bf16"), wl.QGZ_SINGLE_HOP),
+            ("qgz_int8ef_fused", "int8ef_fused",
+             lambda w: run_qgz_fused(w, sub, dev, dist, ws, ef_kind="int8"), wl.QGZ_SINGLE_HOP)):
         line, _ = runner(w)
         torch.cuda.empty_cache()
         out[name] = entry(line, variant_parity_on_sample(w, variant, 64, 2, dev) if check else None)
@@ -1221,7 +1252,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qgz_single_hop",
                     choices=["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef",
-                             "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused", "qgz_tiny",
+                             "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused",
+                             "qgz_bf16ef_fused", "qgz_int8ef_fused", "qgz_tiny",
                              "qgz_hierarchical", "qwz", "sr", "all"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1254,8 +1286,8 @@ def main(argv=None):
     binding.load()                            # fail loudly if the library is missing
     dist = init_dist(ws, True)
     names = (["qgz_single_hop", "qgz_fused", "qgz_bf16ef", "qgz_int8ef", "qgz_tiny",
-              "qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused", "qwz",
-              "sr"]
+              "qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused",
+              "qgz_bf16ef_fused", "qgz_int8ef_fused", "qwz", "sr"]
              if args.workload == "all" else [args.workload])
     for name in names:
         if name == "qgz_hier_ef":
@@ -1264,9 +1296,11 @@ def main(argv=None):
         elif name in ("qgz_bf16ef", "qgz_int8ef"):
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
             line, _ = run_qgz(w, args, dev, dist, ws, ef=name[4:8])
-        elif name == "qgz_fused":
+        elif name in ("qgz_fused", "qgz_bf16ef_fused", "qgz_int8ef_fused"):
             w = wl.QGZ_SINGLE_HOP if args.scale == 1 else qgz_sample(wl.QGZ_SINGLE_HOP, args.scale)
-            line, _ = run_qgz_fused(w, args, dev, dist, ws)
+            line, _ = run_qgz_fused(w, args, dev, dist, ws,
+                                    ef_kind={"qgz_fused": "fp32", "qgz_bf16ef_fused": "bf16",
+                                             "qgz_int8ef_fused": "int8"}[name])
         elif name in ("qgz_hier_fused", "qgz_hier_ef_fused"):
             w = (wl.QGZ_HIERARCHICAL if args.scale == 1
                  else qgz_sample(wl.QGZ_HIERARCHICAL, args.scale))

@@ -221,6 +221,26 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes,
                              void *out, int out_dtype, void *stream);
 
 /*
+ * wc_qgz_step_fused_bf16ef / _int8ef -- wc_qgz_step_fused with the error
+ * buffer of wc_ef_quant_int4_bf16ef (ef16: [R][N] bf16, in place) or of
+ * wc_ef_quant_int4_int8ef (ef8: [R][N] int8 codes, ef8_scales: [R][N/B]
+ * fp32, gradient order, in place): out, codes, scales and the buffer are
+ * bit-identical to calling that quantization and wc_dequant_reduce in
+ * sequence ("Merge LoCo with Zero++", Overview: the error buffer's memory is
+ * LoCo's cost).  The buffer is required (no NULL); the other arguments and
+ * requirements are wc_qgz_step_fused's.
+ */
+WC_API int wc_qgz_step_fused_bf16ef(const uint16_t *g, uint16_t *ef16, uint8_t *codes,
+                                    float *scales, int64_t N, int R, int B,
+                                    float err_scale, float err_beta, float out_scale,
+                                    void *out, int out_dtype, void *stream);
+WC_API int wc_qgz_step_fused_int8ef(const uint16_t *g, int8_t *ef8, float *ef8_scales,
+                                    uint8_t *codes, float *scales, int64_t N, int R,
+                                    int B, float err_scale, float err_beta,
+                                    float out_scale, void *out, int out_dtype,
+                                    void *stream);
+
+/*
  * wc_qgz_first_hop_fused -- the hierarchical step's first stage in one
  * kernel: every rank's error-feedback quantization (wc_ef_quant_int4 with
  * G groups) and the first, intra-group hop (wc_dequant_reduce_requant)
@@ -252,6 +272,26 @@ WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
                                   float err_scale, float err_beta,
                                   uint8_t *out_codes, float *out_scales,
                                   float *ef1, void *stream);
+
+/*
+ * wc_qgz_first_hop_fused_bf16ef / _int8ef -- wc_qgz_first_hop_fused with the
+ * ranks' error buffer of wc_ef_quant_int4_bf16ef (ef16) or of
+ * wc_ef_quant_int4_int8ef (ef8, ef8_scales), as in wc_qgz_step_fused_bf16ef
+ * / _int8ef; bit-identical to that quantization followed by
+ * wc_dequant_reduce_requant (or wc_dequant_reduce_requant_ef with ef1).  The
+ * buffer is required; the other arguments are wc_qgz_first_hop_fused's.
+ */
+WC_API int wc_qgz_first_hop_fused_bf16ef(const uint16_t *g, uint16_t *ef16,
+                                         uint8_t *codes, float *scales, int64_t N,
+                                         int R, int G, int B, float err_scale,
+                                         float err_beta, uint8_t *out_codes,
+                                         float *out_scales, float *ef1, void *stream);
+WC_API int wc_qgz_first_hop_fused_int8ef(const uint16_t *g, int8_t *ef8,
+                                         float *ef8_scales, uint8_t *codes,
+                                         float *scales, int64_t N, int R, int G, int B,
+                                         float err_scale, float err_beta,
+                                         uint8_t *out_codes, float *out_scales,
+                                         float *ef1, void *stream);
 
 /*
  * wc_qwz_quant_int8 -- qwZ block weight quantization.

@@ -153,6 +153,51 @@ def test_fused_step_argument_errors(lib):
     assert call(N=0, g=None, out=None) == binding.WC_OK
 
 
+def test_fused_low_precision_error_buffer_argument_errors(lib):
+    """The bf16 and int8 error-buffer forms of both fused entry points: the
+    buffer (and the int8 scales) are required and 16-byte aligned.  Every
+    call here fails its checks before any launch."""
+    def caller(f, ok, names):
+        def call(**kw):
+            a = list(ok)
+            for k, v in kw.items():
+                a[names.index(k)] = v
+            return f(*a)
+        return call
+    step16 = caller(lib.wc_qgz_step_fused_bf16ef,
+                    (FAKE, FAKE, FAKE, FAKE, 8192, 8, 256, 1.0, 0.5, 1.0, FAKE, 0, None),
+                    ["g", "ef", "codes", "scales", "N", "R", "B", "s", "beta", "os", "out", "dt",
+                     "st"])
+    step8 = caller(lib.wc_qgz_step_fused_int8ef,
+                   (FAKE, FAKE, FAKE, FAKE, FAKE, 8192, 8, 256, 1.0, 0.5, 1.0, FAKE, 0, None),
+                   ["g", "ef", "es", "codes", "scales", "N", "R", "B", "s", "beta", "os", "out",
+                    "dt", "st"])
+    hop16 = caller(lib.wc_qgz_first_hop_fused_bf16ef,
+                   (FAKE, FAKE, FAKE, FAKE, 16 * 512, 8, 2, 256, 1.0, 0.5, FAKE, FAKE, None, None),
+                   ["g", "ef", "codes", "scales", "N", "R", "G", "B", "s", "beta", "oc", "os",
+                    "ef1", "st"])
+    hop8 = caller(lib.wc_qgz_first_hop_fused_int8ef,
+                  (FAKE, FAKE, FAKE, FAKE, FAKE, 16 * 512, 8, 2, 256, 1.0, 0.5, FAKE, FAKE, None,
+                   None),
+                  ["g", "ef", "es", "codes", "scales", "N", "R", "G", "B", "s", "beta", "oc",
+                   "os", "ef1", "st"])
+    for call in (step16, step8, hop16, hop8):
+        assert call(ef=None) == binding.WC_EINVAL          # the buffer is required
+        assert call(ef=MIS) == binding.WC_EALIGN
+        assert call(B=64) == binding.WC_EINVAL
+        assert call(codes=None) == binding.WC_EINVAL       # codes without scales
+        assert call(g=None) == binding.WC_EINVAL
+    for call in (step8, hop8):
+        assert call(es=None) == binding.WC_EINVAL          # int8 needs its block scales
+        assert call(es=MIS) == binding.WC_EALIGN
+    for call in (step16, step8):
+        assert call(dt=3) == binding.WC_EINVAL
+        assert call(N=0, g=None, ef=None, out=None) == binding.WC_OK
+    for call in (hop16, hop8):
+        assert call(ef1=MIS) == binding.WC_EALIGN
+        assert call(N=0, g=None, ef=None, oc=None, os=None) == binding.WC_OK
+
+
 def test_fused_first_hop_argument_errors(lib):
     f = lib.wc_qgz_first_hop_fused
     ok = (FAKE, FAKE, FAKE, FAKE, 16 * 512, 8, 2, 256, 1.0, 0.5, FAKE, FAKE, None, None)

@@ -27,7 +27,8 @@ def test_other_workloads_summary(monkeypatch):
     dev = torch.device("cuda", 0)
     out = bench.other_workloads(args, dev, None, 1, 0)
     assert set(out) == {"qgz_hierarchical", "qgz_hier_ef", "qgz_hier_fused", "qgz_hier_ef_fused",
-                        "qgz_bf16ef", "qgz_int8ef", "qgz_fused", "qwz", "sr"}
+                        "qgz_bf16ef", "qgz_int8ef", "qgz_fused", "qgz_bf16ef_fused",
+                        "qgz_int8ef_fused", "qwz", "sr"}
     want_kernels = {
         "qgz_hierarchical": {"ef_quant_int4", "dequant_reduce_requant", "dequant_reduce"},
         "qgz_hier_ef": {"ef_quant_int4", "dequant_reduce_requant", "dequant_reduce"},
@@ -36,6 +37,8 @@ def test_other_workloads_summary(monkeypatch):
         "qgz_bf16ef": {"ef_quant_int4", "dequant_reduce"},
         "qgz_int8ef": {"ef_quant_int4", "dequant_reduce"},
         "qgz_fused": {"qgz_step_fused"},
+        "qgz_bf16ef_fused": {"qgz_step_fused"},
+        "qgz_int8ef_fused": {"qgz_step_fused"},
         "qwz": {"qwz_quant_int8", "qwz_dequant_int8", "qwz_quant_replica_int8"},
         "sr": {"sr_accumulate"},
     }

@@ -53,7 +53,7 @@ def test_parity_suites_stay_in_bounds(checked_env):
                            "-p", "no:cacheprovider", "tests/test_parity_qgz.py",
                            "tests/test_parity_secondary.py", "tests/test_parity_next.py",
                            "tests/test_parity_sweep.py", "tests/test_parity_packed.py",
-                           "tests/test_parity_fused_hier.py"],
+                           "tests/test_parity_fused_hier.py", "tests/test_parity_fused_lowp.py"],
                           cwd=ROOT, env=checked_env, capture_output=True, text=True,
                           timeout=1800)
     assert proc.returncode == 0, proc.stdout[-4000:] + proc.stderr[-2000:]

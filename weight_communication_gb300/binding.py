@@ -32,7 +32,12 @@ SIGNATURES = {
     "wc_dequant_reduce_requant": [_P, _P, _I64, _I, _I, _I, _P, _P, _P],
     "wc_dequant_reduce_requant_ef": [_P, _P, _I64, _I, _I, _I, _P, _P, _P, _F, _F, _P],
     "wc_qgz_step_fused": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
+    "wc_qgz_step_fused_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
+    "wc_qgz_step_fused_int8ef": [_P, _P, _P, _P, _P, _I64, _I, _I, _F, _F, _F, _P, _I, _P],
     "wc_qgz_first_hop_fused": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P, _P, _P, _P],
+    "wc_qgz_first_hop_fused_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P, _P, _P, _P],
+    "wc_qgz_first_hop_fused_int8ef": [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P, _P, _P,
+                                      _P],
     "wc_ef_quant_int4_bf16ef": [_P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_ef_quant_int4_int8ef": [_P, _P, _P, _P, _P, _I64, _I, _I, _I, _F, _F, _P],
     "wc_qwz_quant_int8": [_P, _P, _P, _I64, _I, _P],
@@ -195,12 +200,33 @@ def dequant_reduce_requant_ef(codes: torch.Tensor, scales: torch.Tensor, out_cod
           _dev(ef1, "ef1", torch.float32, G * N, d), err_scale, err_beta, _stream(codes, stream))
 
 
+def _fused_error(ef: torch.Tensor | None, ef_scales: torch.Tensor | None, n: int, B: int, d):
+    """The fused entry point's suffix and error-buffer pointers for ef's
+    dtype: fp32 (or None), bf16, or int8 with its block scales."""
+    if ef is None or ef.dtype == torch.float32:
+        if ef_scales is not None:
+            raise ValueError("ef_scales goes with an int8 error buffer only")
+        return "", [_dev(ef, "ef", torch.float32, n, d)]
+    if ef.dtype == torch.bfloat16:
+        if ef_scales is not None:
+            raise ValueError("ef_scales goes with an int8 error buffer only")
+        return "_bf16ef", [_dev(ef, "ef", torch.bfloat16, n, d)]
+    if ef.dtype == torch.int8:
+        if ef_scales is None:
+            raise ValueError("an int8 error buffer needs ef_scales")
+        return "_int8ef", [_dev(ef, "ef", torch.int8, n, d),
+                           _dev(ef_scales, "ef_scales", torch.float32, n // B, d)]
+    raise TypeError(f"ef must be float32, bfloat16 or int8, got {ef.dtype}")
+
+
 def qgz_step_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor | None,
                    scales: torch.Tensor | None, out: torch.Tensor, N: int, R: int, B: int,
                    err_scale: float = 1.0, err_beta: float = 0.0, out_scale: float = 1.0,
-                   stream=None) -> None:
-    """wc_qgz_step_fused: flat EF-quant + dequant-reduce in one kernel.
-    codes/scales (the send buffers) may both be None to skip writing them."""
+                   stream=None, ef_scales: torch.Tensor | None = None) -> None:
+    """wc_qgz_step_fused (fp32 or no error buffer), _bf16ef (bf16 ef) or
+    _int8ef (int8 ef with fp32 ef_scales [R*N/B]): flat EF-quant +
+    dequant-reduce in one kernel.  codes/scales (the send buffers) may both be
+    None to skip writing them."""
     d = g.device
     if out.dtype == torch.float32:
         od = WC_F32
@@ -208,8 +234,8 @@ def qgz_step_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.Tensor
         od = WC_BF16
     else:
         raise TypeError("out must be float32 or bfloat16")
-    _call(d, "wc_qgz_step_fused", _dev(g, "g", torch.bfloat16, R * N, d),
-          _dev(ef, "ef", torch.float32, R * N, d),
+    suffix, err = _fused_error(ef, ef_scales, R * N, B, d)
+    _call(d, "wc_qgz_step_fused" + suffix, _dev(g, "g", torch.bfloat16, R * N, d), *err,
           _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, B, err_scale, err_beta,
           out_scale, _dev(out, "out", out.dtype, N, d), od, _stream(g, stream))
@@ -219,14 +245,16 @@ def qgz_first_hop_fused(g: torch.Tensor, ef: torch.Tensor | None, codes: torch.T
                         scales: torch.Tensor | None, out_codes: torch.Tensor,
                         out_scales: torch.Tensor, N: int, R: int, G: int, B: int,
                         err_scale: float = 1.0, err_beta: float = 0.0, stream=None,
-                        ef1: torch.Tensor | None = None) -> None:
-    """wc_qgz_first_hop_fused: every rank's EF-quant and the first hop in one
-    kernel.  codes/scales (the send buffers) may both be None to skip writing
-    them; out_codes/out_scales receive the first hop's output; ef1 (fp32
-    [G*N], or None) is the first hop's own error buffer."""
+                        ef1: torch.Tensor | None = None,
+                        ef_scales: torch.Tensor | None = None) -> None:
+    """wc_qgz_first_hop_fused (fp32 or no error buffer), _bf16ef or _int8ef
+    (by ef's dtype, as qgz_step_fused): every rank's EF-quant and the first
+    hop in one kernel.  codes/scales (the send buffers) may both be None to
+    skip writing them; out_codes/out_scales receive the first hop's output;
+    ef1 (fp32 [G*N], or None) is the first hop's own error buffer."""
     d = g.device
-    _call(d, "wc_qgz_first_hop_fused", _dev(g, "g", torch.bfloat16, R * N, d),
-          _dev(ef, "ef", torch.float32, R * N, d),
+    suffix, err = _fused_error(ef, ef_scales, R * N, B, d)
+    _call(d, "wc_qgz_first_hop_fused" + suffix, _dev(g, "g", torch.bfloat16, R * N, d), *err,
           _dev(codes, "codes", torch.uint8, R * N // 2, d),
           _dev(scales, "scales", torch.float32, R * N // B, d), N, R, G, B, err_scale, err_beta,
           _dev(out_codes, "out_codes", torch.uint8, G * N // 2, d),

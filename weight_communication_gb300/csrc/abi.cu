@@ -185,10 +185,12 @@ WC_API int wc_dequant_reduce_requant_ef(const uint8_t *codes, const float *scale
                      fn);
 }
 
-WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
-                             int64_t N, int R, int B, float err_scale, float err_beta,
-                             float out_scale, void *out, int out_dtype, void *stream) {
-    static const char *fn = "wc_qgz_step_fused";
+// The fused step's checks and launch for every error-buffer form (ef_mode:
+// the buffer's form; ef_needed: the entry point takes no NULL buffer).
+static int fused_step(const char *fn, const uint16_t *g, void *ef, int ef_mode, bool ef_needed,
+                      float *ef_scales, uint8_t *codes, float *scales, int64_t N, int R, int B,
+                      float err_scale, float err_beta, float out_scale, void *out, int out_dtype,
+                      void *stream) {
     wc::QgzGeometry geo;
     int rc = qgz_geometry(fn, N, R, 1, B, &geo);
     if (rc != WC_OK) return rc;
@@ -200,20 +202,47 @@ WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes, float
     if (N == 0) return WC_OK;
     WC_REQUIRE_PTR(fn, g);
     WC_REQUIRE_PTR(fn, out);
+    if (ef_needed) WC_REQUIRE_PTR(fn, ef);
     if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
+    if (ef_mode == wc::kEfModeInt8) WC_REQUIRE_PTR(fn, ef_scales);
     if (codes != nullptr && (!aligned16(codes) || !aligned16(scales)))
         return fail(WC_EALIGN, "%s: codes or scales is not 16-byte aligned", fn);
-    return from_cuda(wc::launch_qgz_fused_step(g, ef, codes, scales, geo, B, err_scale, err_beta,
-                                               out_scale, out, out_dtype == WC_BF16,
+    return from_cuda(wc::launch_qgz_fused_step(g, ef, ef_mode, ef_scales, codes, scales, geo, B,
+                                               err_scale, err_beta, out_scale, out,
+                                               out_dtype == WC_BF16,
                                                static_cast<cudaStream_t>(stream)),
                      fn);
 }
 
-WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
-                                  int64_t N, int R, int G, int B, float err_scale,
-                                  float err_beta, uint8_t *out_codes, float *out_scales,
-                                  float *ef1, void *stream) {
-    static const char *fn = "wc_qgz_first_hop_fused";
+WC_API int wc_qgz_step_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                             int64_t N, int R, int B, float err_scale, float err_beta,
+                             float out_scale, void *out, int out_dtype, void *stream) {
+    return fused_step("wc_qgz_step_fused", g, ef, wc::kEfModeF32, false, nullptr, codes, scales,
+                      N, R, B, err_scale, err_beta, out_scale, out, out_dtype, stream);
+}
+
+WC_API int wc_qgz_step_fused_bf16ef(const uint16_t *g, uint16_t *ef16, uint8_t *codes,
+                                    float *scales, int64_t N, int R, int B, float err_scale,
+                                    float err_beta, float out_scale, void *out, int out_dtype,
+                                    void *stream) {
+    return fused_step("wc_qgz_step_fused_bf16ef", g, ef16, wc::kEfModeBf16, true, nullptr, codes,
+                      scales, N, R, B, err_scale, err_beta, out_scale, out, out_dtype, stream);
+}
+
+WC_API int wc_qgz_step_fused_int8ef(const uint16_t *g, int8_t *ef8, float *ef8_scales,
+                                    uint8_t *codes, float *scales, int64_t N, int R, int B,
+                                    float err_scale, float err_beta, float out_scale, void *out,
+                                    int out_dtype, void *stream) {
+    return fused_step("wc_qgz_step_fused_int8ef", g, ef8, wc::kEfModeInt8, true, ef8_scales,
+                      codes, scales, N, R, B, err_scale, err_beta, out_scale, out, out_dtype,
+                      stream);
+}
+
+// The fused first stage's checks and launch for every error-buffer form.
+static int first_hop_fused(const char *fn, const uint16_t *g, void *ef, int ef_mode,
+                           bool ef_needed, float *ef_scales, uint8_t *codes, float *scales,
+                           int64_t N, int R, int G, int B, float err_scale, float err_beta,
+                           uint8_t *out_codes, float *out_scales, float *ef1, void *stream) {
     wc::QgzGeometry geo;
     int rc = qgz_geometry(fn, N, R, G, B, &geo);
     if (rc != WC_OK) return rc;
@@ -226,16 +255,46 @@ WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes, 
     WC_REQUIRE_PTR(fn, g);
     WC_REQUIRE_PTR(fn, out_codes);
     WC_REQUIRE_PTR(fn, out_scales);
+    if (ef_needed) WC_REQUIRE_PTR(fn, ef);
     if (ef != nullptr && !aligned16(ef)) return fail(WC_EALIGN, "%s: ef is not 16-byte aligned", fn);
+    if (ef_mode == wc::kEfModeInt8) WC_REQUIRE_PTR(fn, ef_scales);
     if (codes != nullptr && (!aligned16(codes) || !aligned16(scales)))
         return fail(WC_EALIGN, "%s: codes or scales is not 16-byte aligned", fn);
     if (!aligned16(out_codes) || !aligned16(out_scales))
         return fail(WC_EALIGN, "%s: out_codes or out_scales is not 16-byte aligned", fn);
     if (ef1 != nullptr && !aligned16(ef1)) return fail(WC_EALIGN, "%s: ef1 is not 16-byte aligned", fn);
-    return from_cuda(wc::launch_qgz_first_hop_fused(g, ef, codes, scales, geo, B, err_scale,
-                                                    err_beta, out_codes, out_scales, ef1,
-                                                    static_cast<cudaStream_t>(stream)),
+    return from_cuda(wc::launch_qgz_first_hop_fused(g, ef, ef_mode, ef_scales, codes, scales, geo,
+                                                    B, err_scale, err_beta, out_codes, out_scales,
+                                                    ef1, static_cast<cudaStream_t>(stream)),
                      fn);
+}
+
+WC_API int wc_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
+                                  int64_t N, int R, int G, int B, float err_scale,
+                                  float err_beta, uint8_t *out_codes, float *out_scales,
+                                  float *ef1, void *stream) {
+    return first_hop_fused("wc_qgz_first_hop_fused", g, ef, wc::kEfModeF32, false, nullptr, codes,
+                           scales, N, R, G, B, err_scale, err_beta, out_codes, out_scales, ef1,
+                           stream);
+}
+
+WC_API int wc_qgz_first_hop_fused_bf16ef(const uint16_t *g, uint16_t *ef16, uint8_t *codes,
+                                         float *scales, int64_t N, int R, int G, int B,
+                                         float err_scale, float err_beta, uint8_t *out_codes,
+                                         float *out_scales, float *ef1, void *stream) {
+    return first_hop_fused("wc_qgz_first_hop_fused_bf16ef", g, ef16, wc::kEfModeBf16, true,
+                           nullptr, codes, scales, N, R, G, B, err_scale, err_beta, out_codes,
+                           out_scales, ef1, stream);
+}
+
+WC_API int wc_qgz_first_hop_fused_int8ef(const uint16_t *g, int8_t *ef8, float *ef8_scales,
+                                         uint8_t *codes, float *scales, int64_t N, int R, int G,
+                                         int B, float err_scale, float err_beta,
+                                         uint8_t *out_codes, float *out_scales, float *ef1,
+                                         void *stream) {
+    return first_hop_fused("wc_qgz_first_hop_fused_int8ef", g, ef8, wc::kEfModeInt8, true,
+                           ef8_scales, codes, scales, N, R, G, B, err_scale, err_beta, out_codes,
+                           out_scales, ef1, stream);
 }
 
 static int qwz_sizes(const char *fn, int64_t n, int B) {

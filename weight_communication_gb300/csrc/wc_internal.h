@@ -33,16 +33,19 @@ cudaError_t launch_dequant_reduce_requant(const uint8_t *codes, const float *sca
                                           uint8_t *out_codes, float *out_scales,
                                           const QgzGeometry &geo, int B, float *ef1, float s,
                                           float beta, cudaStream_t stream);
-cudaError_t launch_qgz_fused_step(const uint16_t *g, float *ef, uint8_t *codes, float *scales,
-                                  const QgzGeometry &geo, int B, float s, float beta,
-                                  float out_scale, void *out, bool out_bf16,
+// ef, ef_mode, ef_scales as in launch_ef_quant_int4; codes/scales: the
+// ranks' send buffers, or both NULL.
+cudaError_t launch_qgz_fused_step(const uint16_t *g, void *ef, int ef_mode, float *ef_scales,
+                                  uint8_t *codes, float *scales, const QgzGeometry &geo, int B,
+                                  float s, float beta, float out_scale, void *out, bool out_bf16,
                                   cudaStream_t stream);
-// codes/scales: the ranks' send buffers, or both NULL; out_codes/out_scales:
-// the first hop's output, as launch_dequant_reduce_requant writes it.
-cudaError_t launch_qgz_first_hop_fused(const uint16_t *g, float *ef, uint8_t *codes,
-                                       float *scales, const QgzGeometry &geo, int B, float s,
-                                       float beta, uint8_t *out_codes, float *out_scales,
-                                       float *ef1, cudaStream_t stream);
+// The same, with out_codes/out_scales the first hop's output as
+// launch_dequant_reduce_requant writes it and ef1 its error buffer or NULL.
+cudaError_t launch_qgz_first_hop_fused(const uint16_t *g, void *ef, int ef_mode,
+                                       float *ef_scales, uint8_t *codes, float *scales,
+                                       const QgzGeometry &geo, int B, float s, float beta,
+                                       uint8_t *out_codes, float *out_scales, float *ef1,
+                                       cudaStream_t stream);
 // replica: bf16 [n] written with the dequantized weights, or NULL.
 cudaError_t launch_qwz_quant_int8(const uint16_t *w, int8_t *codes, float *scales,
                                   uint16_t *replica, uint32_t n, int B, cudaStream_t stream);

@@ -11,8 +11,9 @@ memory and no extra time.
 `QgzReducer` owns the device buffers of one problem (error feedback, send
 buffers, first-hop buffers, reduced shards) and runs a step as 2 launches
 (flat) or 3 launches (hierarchical) on one stream, or, with `fused=True`, as
-1 launch (flat: wc_qgz_step_fused) or 2 (hierarchical: wc_qgz_first_hop_fused,
-then the second hop), bit for bit the same.  `DevicePipeline` overlaps
+1 launch (flat: wc_qgz_step_fused and its bf16/int8-buffer forms) or 2
+(hierarchical: wc_qgz_first_hop_fused and its forms, then the second hop),
+bit for bit the same.  `DevicePipeline` overlaps
 each step's reduce with the next quantization, `HostPipeline` runs steps from
 and to host memory with the copies overlapped, and `GraphedStep` replays a
 step captured in a CUDA graph.
@@ -46,7 +47,7 @@ class QgzReducer:
         with the same err_scale and err_beta.  fused: step() quantizes and
         reduces (flat) or quantizes and runs the first hop, with its error
         buffer if any (hierarchical), in one kernel, still writing the send
-        buffers; it takes an fp32 error buffer or none, and B >= 128."""
+        buffers; it takes every error buffer form, and B >= 128."""
         self.N, self.R, self.G, self.B = N, R, G, B
         self.err_scale, self.err_beta = err_scale, err_beta
         self.out_scale = out_scale
@@ -67,8 +68,6 @@ class QgzReducer:
         self.ef1 = torch.zeros(G * N, dtype=torch.float32, device=dev) if (hop1_ef and G > 1) else None
         self.out = torch.empty(N, dtype=out_dtype, device=dev)
         if fused:
-            if ef_dtype != torch.float32:
-                raise ValueError("fused steps take an fp32 error buffer (or none)")
             if B < 128:
                 raise ValueError(f"fused steps need B >= 128 (one warp per block), got B={B}")
         self.fused = fused
@@ -147,11 +146,11 @@ class QgzReducer:
             binding.qgz_first_hop_fused(g.reshape(-1), self.ef, self.codes, self.scales,
                                         self.codes1, self.scales1, self.N, self.R, self.G,
                                         self.B, self.err_scale, self.err_beta, stream,
-                                        ef1=self.ef1)
+                                        ef1=self.ef1, ef_scales=self.ef_scales)
             return self.reduce_last_hop(stream, out=out)
         binding.qgz_step_fused(g.reshape(-1), self.ef, self.codes, self.scales, out, self.N,
                                self.R, self.B, self.err_scale, self.err_beta, self.out_scale,
-                               stream)
+                               stream, ef_scales=self.ef_scales)
         return out
 
     def step_host(self, g_host: torch.Tensor, g_dev: torch.Tensor, out_host: torch.Tensor,
