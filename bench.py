@@ -192,6 +192,7 @@ class ClockSampler:
 
 KERNEL_SOURCES = {
     "ef_quant_int4": ["weight_communication_gb300/csrc/qgz_quant.cu",
+                      "weight_communication_gb300/csrc/int8_error_block.cuh",
                       "weight_communication_gb300/csrc/wc_device.cuh"],
     "dequant_reduce": ["weight_communication_gb300/csrc/qgz_reduce.cu",
                        "weight_communication_gb300/csrc/wc_device.cuh"],
@@ -204,10 +205,13 @@ KERNEL_SOURCES = {
     "sr_accumulate": ["weight_communication_gb300/csrc/sr_accumulate.cu",
                       "weight_communication_gb300/csrc/wc_device.cuh"],
     "qgz_step_fused": ["weight_communication_gb300/csrc/qgz_fused.cu",
+                      "weight_communication_gb300/csrc/int8_error_block.cuh",
                        "weight_communication_gb300/csrc/wc_device.cuh"],
     "qgz_first_hop_fused": ["weight_communication_gb300/csrc/qgz_fused.cu",
+                           "weight_communication_gb300/csrc/int8_error_block.cuh",
                             "weight_communication_gb300/csrc/wc_device.cuh"],
     "qgz_first_hop_fused_ef1": ["weight_communication_gb300/csrc/qgz_fused.cu",
+                               "weight_communication_gb300/csrc/int8_error_block.cuh",
                                 "weight_communication_gb300/csrc/wc_device.cuh"],
 }
 
