@@ -92,8 +92,10 @@ __device__ __forceinline__ void load_rank_block(const uint16_t *__restrict__ g,
 // values into acc (from +0, in the order the caller visits the ranks).  xr
 // is the block's first gradient element; total = R*N bounds every access.
 // The int8 buffer takes the packed routine of the stand-alone quantization
-// (int8ef_block), the other forms the scalar chain of wc_ef_quant_int4.
-template <int B, int EF, bool WRITE_CODES>
+// (int8ef_block), the other forms the scalar chain of wc_ef_quant_int4.  S1:
+// the error scale s is 1, so s*e is e itself (exact for every finite e) and
+// its multiply is left out.
+template <int B, int EF, bool WRITE_CODES, bool S1>
 __device__ __forceinline__ void quantize_rank_block(
     const uint2 (&gv)[B / 128], const float4 (&er)[B / 128], float es, float (&acc)[B / 128][4],
     void *__restrict__ ef, float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
@@ -104,7 +106,7 @@ __device__ __forceinline__ void quantize_rank_block(
         uint32_t e8w[K];
 #pragma unroll
         for (int k = 0; k < K; ++k) e8w[k] = __float_as_uint(er[k].x);
-        int8ef_block<B, false, WRITE_CODES, true>(gv, e8w, es, static_cast<int8_t *>(ef),
+        int8ef_block<B, S1, WRITE_CODES, true>(gv, e8w, es, static_cast<int8_t *>(ef),
                                                   ef_scales, codes, scales, total, xr, cr, lane,
                                                   s, beta, one_minus_beta, ops, acc);
     } else {
@@ -121,7 +123,7 @@ __device__ __forceinline__ void quantize_rank_block(
             decode_error<EF>(er[k], e[k]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                c[k][j] = HAS_EF ? __fadd_rn(gf[j], __fmul_rn(s, e[k][j])) : gf[j];
+                c[k][j] = HAS_EF ? __fadd_rn(gf[j], S1 ? e[k][j] : __fmul_rn(s, e[k][j])) : gf[j];
                 m = fmaxf(m, fabsf(c[k][j]));
             }
         }
@@ -173,7 +175,7 @@ constexpr int fused_step_min_ctas() {
     return B > 256 ? 1 : EF == kEfModeBf16 ? 6 : EF == kEfModeInt8 ? 4 : 1;
 }
 
-template <int B, int EF, bool WRITE_CODES, bool OUT_BF16>
+template <int B, int EF, bool WRITE_CODES, bool OUT_BF16, bool S1>
 __global__ void __launch_bounds__(256, fused_step_min_ctas<B, EF>())
 qgz_fused_step_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef,
                       float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
@@ -205,8 +207,9 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef,
         float esn = 0.0f;
         if (r + 1 < geo.R)  // prefetch rank r + 1
             load_rank_block<B, EF>(g, ef, ef_scales, xr + geo.N, geo.total, lane, gn, en, esn);
-        quantize_rank_block<B, EF, WRITE_CODES>(gv, er, es, acc, ef, ef_scales, codes, scales, xr,
-                                                xr, geo.total, lane, s, beta, one_minus_beta, ops);
+        quantize_rank_block<B, EF, WRITE_CODES, S1>(gv, er, es, acc, ef, ef_scales, codes, scales,
+                                                    xr, xr, geo.total, lane, s, beta,
+                                                    one_minus_beta, ops);
         if (r + 1 < geo.R) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -235,7 +238,7 @@ qgz_fused_step_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef,
     }
 }
 
-template <int B, int EF, bool WRITE_CODES>
+template <int B, int EF, bool WRITE_CODES, bool S1>
 static cudaError_t launch_fused_3(const uint16_t *g, void *ef, float *ef_scales, uint8_t *codes,
                                   float *scales, const QgzGeometry &geo, float s, float beta,
                                   float out_scale, void *out, bool out_bf16, cudaStream_t stream) {
@@ -244,24 +247,44 @@ static cudaError_t launch_fused_3(const uint16_t *g, void *ef, float *ef_scales,
     const uint32_t grid = (items + threads / kWarp - 1) / (threads / kWarp);
     const float omb = 1.0f - beta;
     if (out_bf16)
-        qgz_fused_step_kernel<B, EF, WRITE_CODES, true><<<grid, threads, 0, stream>>>(
+        qgz_fused_step_kernel<B, EF, WRITE_CODES, true, S1><<<grid, threads, 0, stream>>>(
             g, ef, ef_scales, codes, scales, geo, s, beta, omb, out_scale, out,
             exact2_constants());
     else
-        qgz_fused_step_kernel<B, EF, WRITE_CODES, false><<<grid, threads, 0, stream>>>(
+        qgz_fused_step_kernel<B, EF, WRITE_CODES, false, S1><<<grid, threads, 0, stream>>>(
             g, ef, ef_scales, codes, scales, geo, s, beta, omb, out_scale, out,
             exact2_constants());
     return cudaPeekAtLastError();
+}
+
+// The low-precision buffers' forms are issue-bound, so they also come in a
+// form for s = 1; the fp32 form is HBM-bound and takes the general one.
+template <int EF>
+constexpr bool has_s1_form() {
+    return EF == kEfModeBf16 || EF == kEfModeInt8;
+}
+
+template <int B, int EF, bool S1>
+static cudaError_t launch_fused_s(const uint16_t *g, void *ef, float *ef_scales, uint8_t *codes,
+                                  float *scales, const QgzGeometry &geo, float s, float beta,
+                                  float out_scale, void *out, bool out_bf16, cudaStream_t stream) {
+    if (codes)
+        return launch_fused_3<B, EF, true, S1>(g, ef, ef_scales, codes, scales, geo, s, beta,
+                                               out_scale, out, out_bf16, stream);
+    return launch_fused_3<B, EF, false, S1>(g, ef, ef_scales, codes, scales, geo, s, beta,
+                                            out_scale, out, out_bf16, stream);
 }
 
 template <int B, int EF>
 static cudaError_t launch_fused_2(const uint16_t *g, void *ef, float *ef_scales, uint8_t *codes,
                                   float *scales, const QgzGeometry &geo, float s, float beta,
                                   float out_scale, void *out, bool out_bf16, cudaStream_t stream) {
-    if (codes)
-        return launch_fused_3<B, EF, true>(g, ef, ef_scales, codes, scales, geo, s, beta,
-                                           out_scale, out, out_bf16, stream);
-    return launch_fused_3<B, EF, false>(g, ef, ef_scales, codes, scales, geo, s, beta, out_scale,
+    if constexpr (has_s1_form<EF>()) {
+        if (s == 1.0f)
+            return launch_fused_s<B, EF, true>(g, ef, ef_scales, codes, scales, geo, s, beta,
+                                               out_scale, out, out_bf16, stream);
+    }
+    return launch_fused_s<B, EF, false>(g, ef, ef_scales, codes, scales, geo, s, beta, out_scale,
                                         out, out_bf16, stream);
 }
 
@@ -311,7 +334,7 @@ static cudaError_t launch_fused_b(const uint16_t *g, void *ef, int ef_mode, floa
 // budget for three CTAs of 256 threads per SM (80 registers, a 12-byte spill
 // with the fp32 error buffer and codes) keeps more loads in flight than the
 // compiler's own choice of 122 registers: about 1 % faster at B = 512.
-template <int B, int EF, bool WRITE_CODES, bool HAS_EF1>
+template <int B, int EF, bool WRITE_CODES, bool HAS_EF1, bool S1>
 __global__ void __launch_bounds__(256, B <= 512 ? 3 : 1)
 qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef,
                            float *__restrict__ ef_scales, uint8_t *__restrict__ codes,
@@ -350,9 +373,9 @@ qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef
         float esn = 0.0f;
         if (lq + 1 < geo.L)  // prefetch the next local rank's block
             load_rank_block<B, EF>(g, ef, ef_scales, xr + geo.N, geo.total, lane, gn, en, esn);
-        quantize_rank_block<B, EF, WRITE_CODES>(gv, er, es, acc, ef, ef_scales, codes, scales, xr,
-                                                cbase + lq * geo.N, geo.total, lane, s, beta,
-                                                one_minus_beta, ops);
+        quantize_rank_block<B, EF, WRITE_CODES, S1>(gv, er, es, acc, ef, ef_scales, codes, scales,
+                                                    xr, cbase + lq * geo.N, geo.total, lane, s,
+                                                    beta, one_minus_beta, ops);
         if (lq + 1 < geo.L) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
@@ -406,7 +429,7 @@ qgz_first_hop_fused_kernel(const uint16_t *__restrict__ g, void *__restrict__ ef
     if (lane == 0 && WC_IN_BOUNDS(uint64_t(o0 / B) < total_out / B)) __stcs(out_scales + o0 / B, bs.scale);
 }
 
-template <int B, int EF, bool WRITE_CODES, bool HAS_EF1>
+template <int B, int EF, bool WRITE_CODES, bool HAS_EF1, bool S1>
 static cudaError_t launch_first_hop_fused_4(const uint16_t *g, void *ef, float *ef_scales,
                                             uint8_t *codes, float *scales, const QgzGeometry &geo,
                                             float s, float beta, uint8_t *out_codes,
@@ -414,10 +437,29 @@ static cudaError_t launch_first_hop_fused_4(const uint16_t *g, void *ef, float *
     const uint32_t threads = 256;
     const uint32_t warps = geo.S / B;  // blocks per sub-slice
     const dim3 grid((warps + threads / kWarp - 1) / (threads / kWarp), geo.G, geo.R);
-    qgz_first_hop_fused_kernel<B, EF, WRITE_CODES, HAS_EF1><<<grid, threads, 0, stream>>>(
+    qgz_first_hop_fused_kernel<B, EF, WRITE_CODES, HAS_EF1, S1><<<grid, threads, 0, stream>>>(
         g, ef, ef_scales, codes, scales, geo, s, beta, 1.0f - beta, out_codes, out_scales, ef1,
         exact2_constants());
     return cudaPeekAtLastError();
+}
+
+template <int B, int EF, bool S1>
+static cudaError_t launch_first_hop_fused_s(const uint16_t *g, void *ef, float *ef_scales,
+                                            uint8_t *codes, float *scales, const QgzGeometry &geo,
+                                            float s, float beta, uint8_t *out_codes,
+                                            float *out_scales, float *ef1, cudaStream_t stream) {
+    if (codes) {
+        if (ef1)
+            return launch_first_hop_fused_4<B, EF, true, true, S1>(
+                g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+        return launch_first_hop_fused_4<B, EF, true, false, S1>(
+            g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+    }
+    if (ef1)
+        return launch_first_hop_fused_4<B, EF, false, true, S1>(
+            g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+    return launch_first_hop_fused_4<B, EF, false, false, S1>(
+        g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
 }
 
 template <int B, int EF>
@@ -425,18 +467,13 @@ static cudaError_t launch_first_hop_fused_2(const uint16_t *g, void *ef, float *
                                             uint8_t *codes, float *scales, const QgzGeometry &geo,
                                             float s, float beta, uint8_t *out_codes,
                                             float *out_scales, float *ef1, cudaStream_t stream) {
-    if (codes) {
-        if (ef1)
-            return launch_first_hop_fused_4<B, EF, true, true>(
-                g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
-        return launch_first_hop_fused_4<B, EF, true, false>(
-            g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+    if constexpr (has_s1_form<EF>()) {
+        if (s == 1.0f)
+            return launch_first_hop_fused_s<B, EF, true>(g, ef, ef_scales, codes, scales, geo, s,
+                                                         beta, out_codes, out_scales, ef1, stream);
     }
-    if (ef1)
-        return launch_first_hop_fused_4<B, EF, false, true>(
-            g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
-    return launch_first_hop_fused_4<B, EF, false, false>(
-        g, ef, ef_scales, codes, scales, geo, s, beta, out_codes, out_scales, ef1, stream);
+    return launch_first_hop_fused_s<B, EF, false>(g, ef, ef_scales, codes, scales, geo, s, beta,
+                                                  out_codes, out_scales, ef1, stream);
 }
 
 template <int B>
