@@ -23,7 +23,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def lib():
-    srcs = build.sources() + HEADERS
+    csrc = ROOT / "weight_communication_gb300" / "csrc"
+    srcs = build.sources() + HEADERS + sorted(csrc.glob("*.cuh")) + sorted(csrc.glob("*.h"))
     if not build.LIB.exists() or build.LIB.stat().st_mtime < max(p.stat().st_mtime for p in srcs):
         build.build()
     return binding.load()
