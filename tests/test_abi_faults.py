@@ -1,7 +1,9 @@
-"""Seeded single-fault checks of the qgZ entry points' argument validation.
+"""Seeded single-fault checks of every compute entry point's argument
+validation (qgZ, qwZ, SR).
 
 Each case starts from a random valid geometry (R, G | R, B, k blocks per
-shard) with placeholder pointers and breaks exactly one documented rule --
+shard; or n and B) with placeholder pointers and breaks exactly one
+documented rule --
 a geometry rule, a required pointer left NULL or misaligned, an optional
 pointer misaligned, one of a both-or-neither pair missing, a bad output type,
 a block too small for the fused kernels -- and expects that rule's status
@@ -116,3 +118,53 @@ def test_every_single_fault_is_refused(lib, name):
             assert name in msg, (name, what, msg)
             checked += 1
     assert checked > 500
+
+
+# qwZ and SR: parameter names, required pointers.
+SIZE_ENTRIES = {
+    "wc_qwz_quant_int8": (["w", "codes", "scales", "n", "B", "st"], ["w", "codes", "scales"]),
+    "wc_qwz_quant_replica_int8": (["w", "codes", "scales", "rep", "n", "B", "st"],
+                                  ["w", "codes", "scales", "rep"]),
+    "wc_qwz_dequant_int8": (["codes", "scales", "out", "n", "B", "st"],
+                            ["codes", "scales", "out"]),
+    "wc_sr_accumulate_bf16": (["dst", "src", "n", "seed", "step", "st"], ["dst", "src"]),
+}
+
+
+def size_faults(name: str, rng: random.Random):
+    names, required = SIZE_ENTRIES[name]
+    if name.startswith("wc_qwz"):
+        B = 32 << rng.randint(0, 7)
+        a = dict.fromkeys(names, FAKE)
+        a.update(n=B * rng.randint(1, 4096), B=B, st=None)
+        out = [("negative n", {"n": -B}, EINVAL),
+               ("B not a power of two in [32, 4096]",
+                {"B": rng.choice([0, 16, 48, 100, 8192])}, EINVAL),
+               ("B does not divide n", {"n": a["n"] + B // 2}, EINVAL),
+               ("n reaches 2^32", {"n": 1 << 32, "B": 2048}, ERANGE)]
+    else:
+        n = rng.randint(1, 1 << 20)
+        a = {"dst": FAKE, "src": FAKE + ((2 * n + 15) // 16) * 16 + 16, "n": n,
+             "seed": rng.getrandbits(32), "step": rng.randint(0, 7), "st": None}
+        out = [("negative n", {"n": -1}, EINVAL),
+               ("n reaches 2^32", {"n": 1 << 32}, ERANGE),
+               ("dst and src overlap", {"src": FAKE + 16, "n": max(n, 9)}, EINVAL)]
+    for p in required:
+        out += [(f"{p} NULL", {p: None}, EINVAL), (f"{p} misaligned", {p: MIS}, EALIGN)]
+    return {k: a[k] for k in names}, out
+
+
+@pytest.mark.parametrize("name", sorted(SIZE_ENTRIES))
+def test_every_single_size_fault_is_refused(lib, name):
+    rng = random.Random(sum(map(ord, name)))
+    f = getattr(lib, name)
+    checked = 0
+    for _ in range(60):
+        a, cases = size_faults(name, rng)
+        for what, change, want in cases:
+            args = dict(a, **change)
+            rc = f(*args.values())
+            assert rc == want, (name, what, args, rc, lib.wc_last_error())
+            assert name in lib.wc_last_error().decode(), (name, what)
+            checked += 1
+    assert checked > 300
